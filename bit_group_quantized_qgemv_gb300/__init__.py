@@ -1,0 +1,22 @@
+"""GB300-native dequant-fused quantized GEMV (4/2-bit, group 64, planar).
+
+The kernels live in ``libqgemv.so`` (CUDA C++ for sm_103a, built in-tree by
+``bit_group_quantized_qgemv_gb300.build``); ``include/qgemv.h`` declares its C
+ABI.  This package is the thin Python binding over that ABI.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED,
+    QgemvError,
+    decode_attention_seq1,
+    device_status,
+    last_cuda_error,
+    lib,
+    moe_qgemv_combine,
+    moe_workspace_bytes,
+    qgemv_w2g64,
+    qgemv_w4g64,
+    rmsnorm_qgemv,
+    strerror,
+    swiglu_qgemv,
+    version,
+)

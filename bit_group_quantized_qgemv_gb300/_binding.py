@@ -1,0 +1,210 @@
+"""ctypes binding of libqgemv.so: argument marshalling only.
+
+Each function takes torch tensors that already live on the GPU, passes their
+device pointers and shapes to the C ABI of the same name (include/qgemv.h)
+on the current torch stream, and raises ``QgemvError`` on a non-zero status.
+Every step of the computation runs in the library's CUDA kernels; there is
+no fallback: if the library cannot be loaded, importing fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+_SIGS = {
+    "qgemv_w4g64": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "qgemv_w2g64": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "rmsnorm_qgemv": (_I, [_P, _P, _P, _P, _P, _F, _P, _I, _I, _P]),
+    "swiglu_qgemv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _I, _I, _P]),
+    "moe_qgemv_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
+                               _P, _P, _P, _P]),
+    "qgemv_moe_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "decode_attention_seq1": (_I, [_P, _P, _I, _I, _I, _P]),
+    "qgemv_strerror": (ctypes.c_char_p, [_I]),
+    "qgemv_last_cuda_error": (_I, []),
+    "qgemv_device_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "qgemv_version": (_I, []),
+}
+
+#: Names the C header declares (the binding exposes each one).
+EXPORTED = tuple(_SIGS)
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({strerror(status)})")
+
+
+def _load():
+    path = os.environ.get("QGEMV_LIB") or _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libqgemv.so not found at {path}; build it first with "
+            "`python -m bit_group_quantized_qgemv_gb300.build` (needs nvcc)")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = _load()
+
+
+def strerror(status: int) -> str:
+    return lib.qgemv_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise QgemvError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cuda(t, dtypes, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+_CODES = (torch.int32, getattr(torch, "uint32", torch.int32))
+_F16 = (torch.float16,)
+
+
+def _weight(w, name):
+    codes, scales, biases = w
+    return (_cuda(codes, _CODES, name + ".codes"), _cuda(scales, _F16, name + ".scales"),
+            _cuda(biases, _F16, name + ".biases"))
+
+
+def _plain(fn, bits, w, x, y, residual, stream):
+    codes, scales, biases = _weight(w, "w")
+    x = _cuda(x, _F16, "x")
+    N = codes.shape[-2]
+    K = codes.shape[-1] * 32 // bits
+    M = 1 if x.dim() == 1 else x.shape[0]
+    if y is None:
+        y = torch.empty((N,) if x.dim() == 1 else (M, N), dtype=torch.float16, device=x.device)
+    _cuda(y, _F16, "y")
+    _cuda(residual, _F16, "residual")
+    st = fn(_ptr(codes), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K,
+            _ptr(residual), _stream(stream))
+    _check(st, fn.__name__)
+    return y
+
+
+def qgemv_w4g64(w, x, y=None, residual=None, stream=None):
+    """y = W x (+ residual) for a 4-bit g64 weight w = (codes, scales, biases)."""
+    return _plain(lib.qgemv_w4g64, 4, w, x, y, residual, stream)
+
+
+def qgemv_w2g64(w, x, y=None, residual=None, stream=None):
+    """y = W x (+ residual) for a 2-bit g64 weight w = (codes, scales, biases)."""
+    return _plain(lib.qgemv_w2g64, 2, w, x, y, residual, stream)
+
+
+def rmsnorm_qgemv(w, x, norm_weight, eps=1e-5, y=None, stream=None):
+    codes, scales, biases = _weight(w, "w")
+    x = _cuda(x, _F16, "x")
+    _cuda(norm_weight, _F16, "norm_weight")
+    N, K = codes.shape[-2], codes.shape[-1] * 8
+    if y is None:
+        y = torch.empty(N, dtype=torch.float16, device=x.device)
+    st = lib.rmsnorm_qgemv(_ptr(codes), _ptr(scales), _ptr(biases), _ptr(x), _ptr(norm_weight),
+                           float(eps), _ptr(y), N, K, _stream(stream))
+    _check(st, "rmsnorm_qgemv")
+    return y
+
+
+def swiglu_qgemv(gate, up, x, norm_weight=None, eps=1e-5, h=None, stream=None):
+    gc, gs, gb = _weight(gate, "gate")
+    uc, us, ub = _weight(up, "up")
+    x = _cuda(x, _F16, "x")
+    _cuda(norm_weight, _F16, "norm_weight")
+    I, K = gc.shape[-2], gc.shape[-1] * 8
+    if h is None:
+        h = torch.empty(I, dtype=torch.float16, device=x.device)
+    st = lib.swiglu_qgemv(_ptr(gc), _ptr(gs), _ptr(gb), _ptr(uc), _ptr(us), _ptr(ub), _ptr(x),
+                          _ptr(norm_weight), float(eps), _ptr(h), I, K, _stream(stream))
+    _check(st, "swiglu_qgemv")
+    return h
+
+
+def moe_workspace_bytes(top_k: int, inter: int) -> int:
+    return int(lib.qgemv_moe_workspace_bytes(int(top_k), int(inter)))
+
+
+def moe_qgemv_combine(gu, dn, expert_idx, expert_w, x, residual=None, y=None, workspace=None,
+                      err_flag=None, stream=None):
+    """gu = (codes [E][2I][H/8], scales, biases), dn = (codes [E][H][I/8], ...)."""
+    gc, gs, gb = _weight(gu, "gu")
+    dc, ds, db = _weight(dn, "dn")
+    _cuda(expert_idx, (torch.int32,), "expert_idx")
+    _cuda(expert_w, (torch.float32,), "expert_w")
+    x = _cuda(x, _F16, "x")
+    _cuda(residual, _F16, "residual")
+    E, I2, H8 = gc.shape
+    I, H = I2 // 2, H8 * 8
+    top_k = expert_idx.numel()
+    if y is None:
+        y = torch.empty(H, dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(top_k * I, dtype=torch.float32, device=x.device)
+    _cuda(workspace, (torch.float32,), "workspace")
+    _cuda(err_flag, (torch.int32,), "err_flag")
+    st = lib.moe_qgemv_combine(_ptr(gc), _ptr(gs), _ptr(gb), _ptr(dc), _ptr(ds), _ptr(db), E, H,
+                               I, _ptr(expert_idx), _ptr(expert_w), top_k, _ptr(x),
+                               _ptr(residual), _ptr(y), _ptr(workspace), _ptr(err_flag),
+                               _stream(stream))
+    _check(st, "moe_qgemv_combine")
+    return y
+
+
+def decode_attention_seq1(qkv, n_q, n_kv, head_dim, out=None, stream=None):
+    qkv = _cuda(qkv, _F16, "qkv")
+    if out is None:
+        out = torch.empty(n_q * head_dim, dtype=torch.float16, device=qkv.device)
+    st = lib.decode_attention_seq1(_ptr(qkv), _ptr(out), int(n_q), int(n_kv), int(head_dim),
+                                   _stream(stream))
+    _check(st, "decode_attention_seq1")
+    return out
+
+
+def device_status() -> int:
+    """Read and clear the device-side status word (synchronises the device)."""
+    flags = ctypes.c_uint(0)
+    _check(lib.qgemv_device_status(ctypes.byref(flags)), "qgemv_device_status")
+    return int(flags.value)
+
+
+def last_cuda_error() -> int:
+    return int(lib.qgemv_last_cuda_error())
+
+
+def version() -> int:
+    return int(lib.qgemv_version())

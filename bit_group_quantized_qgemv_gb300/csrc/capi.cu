@@ -1,0 +1,282 @@
+// capi.cu -- the extern "C" boundary of libqgemv.so (declared in
+// include/qgemv.h).  Host code only: validates arguments, picks the
+// streaming kernel or the generic kernel, and launches on the caller's
+// stream.  Never allocates, frees or synchronises (except the diagnostic
+// qgemv_device_status).
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/qgemv.h"
+#include "qgemv_args.h"
+
+namespace {
+
+using qgemv::StreamArgs;
+using qgemv::StreamPlan;
+
+thread_local int t_last_cuda_error = 0;
+
+// Multiprocessor count per device, read once.
+std::atomic<int> g_sms[64];
+
+int current_device(int* dev, int* sms) {
+  if (cudaGetDevice(dev) != cudaSuccess) return QGEMV_EDEVICE;
+  if (*dev < 0 || *dev >= 64) return QGEMV_EDEVICE;
+  int v = g_sms[*dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess || v <= 0)
+      return QGEMV_EDEVICE;
+    g_sms[*dev].store(v, std::memory_order_relaxed);
+  }
+  *sms = v;
+  return QGEMV_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int finish(cudaError_t e) {
+  if (e == cudaSuccess) return QGEMV_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return QGEMV_ELAUNCH;
+}
+
+bool valid_k(int K) { return K >= 64 && K % 64 == 0; }
+
+StreamArgs blank_args() {
+  StreamArgs a{};
+  a.M = 1;
+  a.top_k = 1;
+  return a;
+}
+
+int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+               const uint16_t* x, uint16_t* y, int M, int N, int K, const uint16_t* residual,
+               void* stream) {
+  if (!codes || !scales || !biases || !x || !y) return QGEMV_ENULL;
+  if (M < 1 || M > QGEMV_MAX_M || N < 1 || !valid_k(K)) return QGEMV_EINVAL;
+  if (!aligned(codes, 4) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(x, 2) ||
+      !aligned(y, 2) || !aligned(residual, 2))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  StreamArgs a = blank_args();
+  a.codes[0] = reinterpret_cast<const uint8_t*>(codes);
+  a.scales[0] = reinterpret_cast<const __half*>(scales);
+  a.biases[0] = reinterpret_cast<const __half*>(biases);
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = reinterpret_cast<__half*>(y);
+  a.residual = reinterpret_cast<const __half*>(residual);
+  a.rows = N;
+  a.K = K;
+  a.M = M;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms);
+  if (M == 1 && p.ok && aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
+      aligned(x, 16))
+    return finish(qgemv::stream_plain(bits, p, a, st, dev));
+  return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemv_w4g64(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                const uint16_t* x, uint16_t* y, int M, int N, int K, const uint16_t* residual,
+                void* stream) {
+  return plain_impl(4, codes, scales, biases, x, y, M, N, K, residual, stream);
+}
+
+int qgemv_w2g64(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                const uint16_t* x, uint16_t* y, int M, int N, int K, const uint16_t* residual,
+                void* stream) {
+  return plain_impl(2, codes, scales, biases, x, y, M, N, K, residual, stream);
+}
+
+int rmsnorm_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                  const uint16_t* x, const uint16_t* norm_weight, float eps, uint16_t* y, int N,
+                  int K, void* stream) {
+  if (!codes || !scales || !biases || !x || !norm_weight || !y) return QGEMV_ENULL;
+  if (N < 1 || !valid_k(K) || !(eps > 0.0f) || eps > 1e30f) return QGEMV_EINVAL;
+  if (!aligned(codes, 4) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(x, 2) ||
+      !aligned(norm_weight, 2) || !aligned(y, 2))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  StreamArgs a = blank_args();
+  a.codes[0] = reinterpret_cast<const uint8_t*>(codes);
+  a.scales[0] = reinterpret_cast<const __half*>(scales);
+  a.biases[0] = reinterpret_cast<const __half*>(biases);
+  a.x = reinterpret_cast<const __half*>(x);
+  a.gamma = reinterpret_cast<const __half*>(norm_weight);
+  a.eps = eps;
+  a.y = reinterpret_cast<__half*>(y);
+  a.rows = N;
+  a.K = K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const StreamPlan p = qgemv::make_stream_plan(qgemv::kNorm, 4, K, N, 1, sms);
+  if (p.ok && aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
+      aligned(x, 16) && aligned(norm_weight, 16))
+    return finish(qgemv::stream_norm(p, a, st, dev));
+  return finish(qgemv::generic_launch(qgemv::kNorm, 4, a, st));
+}
+
+int swiglu_qgemv(const uint32_t* gate_codes, const uint16_t* gate_scales,
+                 const uint16_t* gate_biases, const uint32_t* up_codes, const uint16_t* up_scales,
+                 const uint16_t* up_biases, const uint16_t* x, const uint16_t* norm_weight,
+                 float eps, uint16_t* h, int I, int K, void* stream) {
+  if (!gate_codes || !gate_scales || !gate_biases || !up_codes || !up_scales || !up_biases ||
+      !x || !h)
+    return QGEMV_ENULL;
+  if (I < 1 || !valid_k(K)) return QGEMV_EINVAL;
+  if (norm_weight && (!(eps > 0.0f) || eps > 1e30f)) return QGEMV_EINVAL;
+  if (!aligned(gate_codes, 4) || !aligned(up_codes, 4) || !aligned(gate_scales, 2) ||
+      !aligned(gate_biases, 2) || !aligned(up_scales, 2) || !aligned(up_biases, 2) ||
+      !aligned(x, 2) || !aligned(norm_weight, 2) || !aligned(h, 2))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  StreamArgs a = blank_args();
+  a.codes[0] = reinterpret_cast<const uint8_t*>(gate_codes);
+  a.scales[0] = reinterpret_cast<const __half*>(gate_scales);
+  a.biases[0] = reinterpret_cast<const __half*>(gate_biases);
+  a.codes[1] = reinterpret_cast<const uint8_t*>(up_codes);
+  a.scales[1] = reinterpret_cast<const __half*>(up_scales);
+  a.biases[1] = reinterpret_cast<const __half*>(up_biases);
+  a.x = reinterpret_cast<const __half*>(x);
+  a.gamma = reinterpret_cast<const __half*>(norm_weight);
+  a.eps = eps;
+  a.y = reinterpret_cast<__half*>(h);
+  a.rows = I;
+  a.K = K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const StreamPlan p = qgemv::make_stream_plan(qgemv::kSwiglu, 4, K, I, 1, sms);
+  if (p.ok && aligned(gate_codes, 16) && aligned(gate_scales, 16) && aligned(gate_biases, 16) &&
+      aligned(up_codes, 16) && aligned(up_scales, 16) && aligned(up_biases, 16) &&
+      aligned(x, 16) && (norm_weight == nullptr || aligned(norm_weight, 16)))
+    return finish(qgemv::stream_swiglu(p, a, st, dev));
+  return finish(qgemv::generic_launch(qgemv::kSwiglu, 4, a, st));
+}
+
+size_t qgemv_moe_workspace_bytes(int top_k, int I) {
+  if (top_k < 1 || I < 1) return 0;
+  return static_cast<size_t>(top_k) * static_cast<size_t>(I) * sizeof(float);
+}
+
+int moe_qgemv_combine(const uint32_t* gu_codes, const uint16_t* gu_scales,
+                      const uint16_t* gu_biases, const uint32_t* dn_codes,
+                      const uint16_t* dn_scales, const uint16_t* dn_biases, int n_experts, int H,
+                      int I, const int32_t* expert_idx, const float* expert_w, int top_k,
+                      const uint16_t* x, const uint16_t* residual, uint16_t* y, float* workspace,
+                      int* err_flag, void* stream) {
+  if (!gu_codes || !gu_scales || !gu_biases || !dn_codes || !dn_scales || !dn_biases ||
+      !expert_idx || !expert_w || !x || !y || !workspace)
+    return QGEMV_ENULL;
+  if (n_experts < 1 || top_k < 1 || top_k > QGEMV_MAX_TOPK || !valid_k(H) || !valid_k(I))
+    return QGEMV_EINVAL;
+  if (!aligned(gu_codes, 4) || !aligned(dn_codes, 4) || !aligned(gu_scales, 2) ||
+      !aligned(gu_biases, 2) || !aligned(dn_scales, 2) || !aligned(dn_biases, 2) ||
+      !aligned(expert_idx, 4) || !aligned(expert_w, 4) || !aligned(x, 2) ||
+      !aligned(residual, 2) || !aligned(y, 2) || !aligned(workspace, 4) || !aligned(err_flag, 4))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long gu_row_bytes = static_cast<long long>(H) / 2;  // 4-bit: H/8 words * 4 B
+  const long long dn_row_bytes = static_cast<long long>(I) / 2;
+
+  // Phase 1: h_k = silu(Wg[e_k] x) * (Wu[e_k] x) into the workspace.
+  StreamArgs u = blank_args();
+  u.codes[0] = reinterpret_cast<const uint8_t*>(gu_codes);
+  u.codes[1] = reinterpret_cast<const uint8_t*>(gu_codes) + static_cast<long long>(I) * gu_row_bytes;
+  u.scales[0] = reinterpret_cast<const __half*>(gu_scales);
+  u.scales[1] = reinterpret_cast<const __half*>(gu_scales) + static_cast<long long>(I) * (H / 64);
+  u.biases[0] = reinterpret_cast<const __half*>(gu_biases);
+  u.biases[1] = reinterpret_cast<const __half*>(gu_biases) + static_cast<long long>(I) * (H / 64);
+  u.ex_code_bytes = 2LL * I * gu_row_bytes;
+  u.ex_groups = 2LL * I * (H / 64);
+  u.x = reinterpret_cast<const __half*>(x);
+  u.yf = workspace;
+  u.idx = expert_idx;
+  u.wt = expert_w;
+  u.err_flag = err_flag;
+  u.top_k = top_k;
+  u.n_experts = n_experts;
+  u.rows = static_cast<long long>(top_k) * I;
+  u.rows_per_expert = I;
+  u.K = H;
+  const StreamPlan pu = qgemv::make_stream_plan(qgemv::kMoeUp, 4, H, u.rows, top_k, sms);
+  cudaError_t e;
+  if (pu.ok && aligned(gu_codes, 16) && aligned(gu_scales, 16) && aligned(gu_biases, 16) &&
+      aligned(x, 16))
+    e = qgemv::stream_moe_up(pu, u, st, dev);
+  else
+    e = qgemv::generic_launch(qgemv::kMoeUp, 4, u, st);
+  if (e != cudaSuccess) return finish(e);
+
+  // Phase 2: y = r + sum_k wt_k Wd[e_k] h_k.
+  StreamArgs d = blank_args();
+  d.codes[0] = reinterpret_cast<const uint8_t*>(dn_codes);
+  d.scales[0] = reinterpret_cast<const __half*>(dn_scales);
+  d.biases[0] = reinterpret_cast<const __half*>(dn_biases);
+  d.ex_code_bytes = static_cast<long long>(H) * dn_row_bytes;
+  d.ex_groups = static_cast<long long>(H) * (I / 64);
+  d.xf = workspace;
+  d.residual = reinterpret_cast<const __half*>(residual);
+  d.y = reinterpret_cast<__half*>(y);
+  d.idx = expert_idx;
+  d.wt = expert_w;
+  d.err_flag = err_flag;
+  d.top_k = top_k;
+  d.n_experts = n_experts;
+  d.rows = H;
+  d.K = I;
+  const StreamPlan pd = qgemv::make_stream_plan(qgemv::kMoeDown, 4, I, H, top_k, sms);
+  if (pd.ok && aligned(dn_codes, 16) && aligned(dn_scales, 16) && aligned(dn_biases, 16) &&
+      aligned(workspace, 16))
+    e = qgemv::stream_moe_down(pd, d, st, dev);
+  else
+    e = qgemv::generic_launch(qgemv::kMoeDown, 4, d, st);
+  return finish(e);
+}
+
+int decode_attention_seq1(const uint16_t* qkv, uint16_t* out, int n_q, int n_kv, int head_dim,
+                          void* stream) {
+  if (!qkv || !out) return QGEMV_ENULL;
+  if (n_q < 1 || n_kv < 1 || head_dim < 1 || n_q % n_kv != 0) return QGEMV_EINVAL;
+  if (!aligned(qkv, 2) || !aligned(out, 2)) return QGEMV_EALIGN;
+  return finish(qgemv::attention_seq1_launch(reinterpret_cast<const __half*>(qkv),
+                                             reinterpret_cast<__half*>(out), n_q, n_kv, head_dim,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+const char* qgemv_strerror(int status) {
+  switch (status) {
+    case QGEMV_OK: return "ok";
+    case QGEMV_EINVAL: return "invalid shape or scalar argument";
+    case QGEMV_ENULL: return "required pointer is NULL";
+    case QGEMV_EALIGN: return "pointer misaligned (codes need 4 bytes, fp16 2 bytes)";
+    case QGEMV_ELAUNCH: return "CUDA reported an error at kernel launch";
+    case QGEMV_EDEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int qgemv_last_cuda_error(void) { return t_last_cuda_error; }
+
+int qgemv_device_status(unsigned* flags) {
+  if (!flags) return QGEMV_ENULL;
+  *flags = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return QGEMV_EDEVICE;
+  unsigned v = 0;
+  if (qgemv::status_plain(&v) != cudaSuccess || qgemv::status_norm_swiglu(&v) != cudaSuccess ||
+      qgemv::status_moe(&v) != cudaSuccess || qgemv::status_generic(&v) != cudaSuccess)
+    return QGEMV_EDEVICE;
+  *flags = v;
+  return QGEMV_OK;
+}
+
+int qgemv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,14 @@
+// Streaming kernels: plain 4-bit and 2-bit GEMV (optionally + residual).
+#include "qgemv_stream.cuh"
+
+namespace qgemv {
+
+cudaError_t stream_plain(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
+                         int device) {
+  if (bits == 4) return launch_stream<4, kPlain>(p, a, st, device);
+  return launch_stream<2, kPlain>(p, a, st, device);
+}
+
+cudaError_t status_plain(unsigned* out) { return read_clear_status(out); }
+
+}  // namespace qgemv

@@ -1,0 +1,177 @@
+/*
+ * qgemv.h -- C ABI of libqgemv.so: dequant-fused quantized matrix-vector
+ * products for batch-1 (and small-batch) LLM decode on NVIDIA GB300 (sm_103a).
+ *
+ * Weight format (all entry points).  A weight W of N rows and K columns is
+ * stored planar, MLX style ("Boosting inference speed on Apple Silicon",
+ * INFERENCE_RESEARCH.md, section 3, item 4: 4-bit data packed in uint32 plus
+ * separate scale and bias tensors, group 64; item 5: rows laid out along the
+ * matvec's access direction, consumed as stored):
+ *   codes   uint32 [N][K*bits/32]  row-major; code q[n][k] sits in word
+ *           k / (32/bits) at bit offset bits * (k % (32/bits)), low bits first.
+ *   scales  fp16   [N][K/64]       row-major, one per 64 consecutive k of a row.
+ *   biases  fp16   [N][K/64]       same layout.
+ *   w[n][k] = q[n][k] * scales[n][k/64] + biases[n][k/64].
+ * fp16 values are IEEE binary16 passed as uint16_t bit patterns.  Activations
+ * x are fp16 [M][K] and outputs fp16 [M][N], row-major, unit stride.  Every
+ * product accumulates in fp32 and each fp16 output is rounded once (RNE).
+ * The inner loop evaluates the dequantised product through the exact
+ * rewrite of (q*scale + bias)*x as fma(q, scale*x, bias*x) given on the
+ * hada.io page (topic 27758), "Noyau de dequantification optimise FMA",
+ * factored per group of 64: scale * sum(q*x) + bias * sum(x).
+ *
+ * Conventions.
+ *   - Every pointer argument except `stream` is a DEVICE pointer owned by
+ *     the caller.  The library never allocates, frees or synchronises; work
+ *     is only enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Return value: QGEMV_OK (0) or a negative QGEMV_E* status.  Argument
+ *     checks run on the host before any launch; on failure nothing is
+ *     enqueued.  QGEMV_ELAUNCH reports a CUDA error seen right after the
+ *     launch; its code is kept for qgemv_last_cuda_error().
+ *   - Kernels never trap.  A device-side wait that runs out (it has a
+ *     bounded spin) sets a library flag read by qgemv_device_status().
+ *   - Inputs may not overlap outputs, except that `residual` may be the
+ *     same pointer as `y` (an in-place residual add).
+ *   - Calls are asynchronous and thread-compatible: concurrent calls on
+ *     different streams are safe when their outputs do not overlap.
+ */
+#ifndef QGEMV_H_
+#define QGEMV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QGEMV_OK 0
+#define QGEMV_EINVAL (-1)  /* bad shape or scalar argument                   */
+#define QGEMV_ENULL (-2)   /* a required pointer is NULL                      */
+#define QGEMV_EALIGN (-3)  /* codes not 4-byte aligned, fp16 not 2-byte aligned */
+#define QGEMV_ELAUNCH (-4) /* CUDA reported an error at launch                */
+#define QGEMV_EDEVICE (-5) /* no usable CUDA device / device query failed     */
+
+/* Largest supported small batch M and expert count top_k. */
+#define QGEMV_MAX_M 8
+#define QGEMV_MAX_TOPK 8
+
+/*
+ * qgemv_w4g64 -- y[m][n] = sum_k w[n][k] * x[m][k] (+ residual[m][n]),
+ * 4-bit codes, group 64.  The dequant-fused GEMV of INFERENCE_RESEARCH.md
+ * section 1 (dequantisation inside the inner loop, no f32 weights ever
+ * materialised); small-batch M <= 8 follows the mat-vec branch of the
+ * "routing by M" decision in the same section.
+ *   codes    [N][K/8] uint32      scales, biases [N][K/64] fp16
+ *   x        [M][K] fp16          y [M][N] fp16
+ *   residual [M][N] fp16 or NULL (may equal y)
+ *   1 <= M <= 8, N >= 1, K >= 64 and K % 64 == 0, else QGEMV_EINVAL.
+ */
+int qgemv_w4g64(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                const uint16_t *x, uint16_t *y, int M, int N, int K,
+                const uint16_t *residual, void *stream);
+
+/*
+ * qgemv_w2g64 -- the same product with 2-bit codes (the 2-bit expert
+ * configuration on the hada.io page, "Resultats de performance" and
+ * "Shaders de calcul Metal"): codes [N][K/16] uint32, 16 codes per word,
+ * low bits first.  Other arguments and checks as qgemv_w4g64.
+ */
+int qgemv_w2g64(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                const uint16_t *x, uint16_t *y, int M, int N, int K,
+                const uint16_t *residual, void *stream);
+
+/*
+ * rmsnorm_qgemv -- y = W . (x * gamma / sqrt(mean(x^2) + eps)), M = 1,
+ * 4-bit g64.  The RMSNorm + QKV matvec fusion of INFERENCE_RESEARCH.md
+ * section 1 (and the RMS normalisation shader on the hada.io page).
+ *   x, norm_weight (gamma) [K] fp16; y [N] fp16; eps > 0 (else EINVAL).
+ * The normalised activation x*gamma is rounded to fp16 once inside the
+ * kernel and 1/sqrt(mean(x^2)+eps) is applied to the fp32 row sums.
+ */
+int rmsnorm_qgemv(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                  const uint16_t *x, const uint16_t *norm_weight, float eps,
+                  uint16_t *y, int N, int K, void *stream);
+
+/*
+ * swiglu_qgemv -- h[i] = silu(g_i) * u_i with g = Wg . xt, u = Wu . xt,
+ * xt = x, or xt = rmsnorm(x) * gamma when norm_weight is not NULL (the
+ * post-attention norm fused in front).  The "gate.up SwiGLU in one kernel"
+ * fusion of INFERENCE_RESEARCH.md section 1; silu(z) = z / (1 + e^-z).
+ *   gate_*: Wg [I][K], up_*: Wu [I][K] (4-bit g64, separate pointers; a
+ *   caller holding one [2I][K] matrix passes base and base + I rows).
+ *   x [K] fp16, norm_weight [K] fp16 or NULL, eps > 0 when used; h [I] fp16.
+ */
+int swiglu_qgemv(const uint32_t *gate_codes, const uint16_t *gate_scales,
+                 const uint16_t *gate_biases, const uint32_t *up_codes,
+                 const uint16_t *up_scales, const uint16_t *up_biases,
+                 const uint16_t *x, const uint16_t *norm_weight, float eps,
+                 uint16_t *h, int I, int K, void *stream);
+
+/*
+ * moe_qgemv_combine -- MoE top-K expert matvec with weighted combine and
+ * residual (hada.io page: 512 experts, K = 4 active per token including one
+ * shared expert, hidden 4096, "Deferred GPU Expert Compute": combine +
+ * residual on the GPU, result handed to the next layer):
+ *   for k < top_k: e = expert_idx[k];
+ *     h_k = silu(Wgu[e][0:I] . x) * (Wgu[e][I:2I] . x)      (fp32, workspace)
+ *   y[n] = residual[n] + sum_k expert_w[k] * (Wd[e] . h_k)[n]   (fp16)
+ *   gu_codes  [E][2I][H/8] uint32, gu_scales/gu_biases [E][2I][H/64] fp16
+ *             (expert-contiguous; gate rows 0..I-1, then up rows I..2I-1)
+ *   dn_codes  [E][H][I/8] uint32, dn_scales/dn_biases [E][H][I/64] fp16
+ *   expert_idx [top_k] int32 and expert_w [top_k] fp32 are DEVICE arrays,
+ *   read by the kernels (no host synchronisation).
+ *   x, residual, y [H] fp16 (residual may equal y; NULL means zero).
+ *   workspace: device fp32, >= qgemv_moe_workspace_bytes(top_k, I) bytes,
+ *   4-byte aligned; its contents on entry are ignored.
+ *   err_flag: device int or NULL.  An index outside [0, n_experts) sets
+ *   *err_flag = 1 and that expert contributes nothing; the flag is never
+ *   cleared by the library.  A repeated index contributes twice.
+ *   Checks: n_experts >= 1, 1 <= top_k <= 8, H and I >= 64, multiples of 64.
+ */
+int moe_qgemv_combine(const uint32_t *gu_codes, const uint16_t *gu_scales,
+                      const uint16_t *gu_biases, const uint32_t *dn_codes,
+                      const uint16_t *dn_scales, const uint16_t *dn_biases,
+                      int n_experts, int H, int I, const int32_t *expert_idx,
+                      const float *expert_w, int top_k, const uint16_t *x,
+                      const uint16_t *residual, uint16_t *y, float *workspace,
+                      int *err_flag, void *stream);
+
+/* Workspace bytes moe_qgemv_combine needs: top_k * I fp32 values. */
+size_t qgemv_moe_workspace_bytes(int top_k, int I);
+
+/*
+ * decode_attention_seq1 -- attention of one query over a single cached
+ * position: the softmax over one score is 1, so query head h returns value
+ * head h / (n_q / n_kv) unchanged.  Copies those value heads out of a fused
+ * QKV vector into the o_proj input:
+ *   out[h*head_dim + d] = qkv[(n_q + n_kv + h / (n_q/n_kv)) * head_dim + d].
+ * qkv [(n_q + 2 n_kv) * head_dim] fp16, out [n_q * head_dim] fp16.
+ * n_q % n_kv == 0 else EINVAL.  (The decode-stack stand-in for attention;
+ * attention proper is outside this library.)
+ */
+int decode_attention_seq1(const uint16_t *qkv, uint16_t *out, int n_q, int n_kv,
+                          int head_dim, void *stream);
+
+/* Human-readable text for a status code (static string). */
+const char *qgemv_strerror(int status);
+
+/* cudaError_t value of the last QGEMV_ELAUNCH on this host thread (0 if none). */
+int qgemv_last_cuda_error(void);
+
+/*
+ * qgemv_device_status -- synchronously read and clear the library's
+ * device-side status word on the current device: bit 0 = a bounded wait in a
+ * kernel ran out.  *flags receives the word.  Diagnostic: it synchronises the
+ * device.  Returns QGEMV_OK or QGEMV_EDEVICE.
+ */
+int qgemv_device_status(unsigned *flags);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int qgemv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H_ */

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/qgemv.h declares, and rejects bad arguments with the
+documented status before touching the device.  Plus the byte accounting."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "qgemv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def q():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_group_quantized_qgemv_gb300 as mod
+    return mod
+
+
+def test_header_lists_the_boundary():
+    names = header_functions()
+    for n in ["qgemv_w4g64", "qgemv_w2g64", "rmsnorm_qgemv", "swiglu_qgemv",
+              "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
+              "decode_attention_seq1", "qgemv_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(q):
+    raw = ctypes.CDLL(q._binding._build.LIB)
+    for name in header_functions():
+        assert hasattr(raw, name), name
+    assert set(header_functions()) <= set(q.EXPORTED)
+
+
+def _fake_ptr(v=0x10000):
+    return ctypes.c_void_p(v)
+
+
+def test_null_pointer_status(q):
+    L = q.lib
+    assert L.qgemv_w4g64(None, _fake_ptr(), _fake_ptr(), _fake_ptr(), _fake_ptr(),
+                         1, 4, 64, None, None) == -2
+    assert L.qgemv_w2g64(_fake_ptr(), _fake_ptr(), _fake_ptr(), None, _fake_ptr(),
+                         1, 4, 64, None, None) == -2
+    assert L.rmsnorm_qgemv(_fake_ptr(), _fake_ptr(), _fake_ptr(), _fake_ptr(), None, 1e-5,
+                           _fake_ptr(), 4, 64, None) == -2
+    assert L.moe_qgemv_combine(*[_fake_ptr()] * 6, 8, 64, 64, None, _fake_ptr(), 4,
+                               _fake_ptr(), None, _fake_ptr(), _fake_ptr(), None, None) == -2
+
+
+@pytest.mark.parametrize("M,N,K", [(0, 4, 64), (9, 4, 64), (1, 0, 64), (1, 4, 0),
+                                   (1, 4, 96), (1, 4, 32), (1, -1, 64)])
+def test_bad_shape_status(q, M, N, K):
+    p = _fake_ptr()
+    assert q.lib.qgemv_w4g64(p, p, p, p, p, M, N, K, None, None) == -1
+    assert q.lib.qgemv_w2g64(p, p, p, p, p, M, N, K, None, None) == -1
+
+
+def test_bad_scalar_status(q):
+    p = _fake_ptr()
+    assert q.lib.rmsnorm_qgemv(p, p, p, p, p, 0.0, p, 4, 64, None) == -1
+    assert q.lib.rmsnorm_qgemv(p, p, p, p, p, -1.0, p, 4, 64, None) == -1
+    assert q.lib.rmsnorm_qgemv(p, p, p, p, p, float("nan"), p, 4, 64, None) == -1
+    assert q.lib.swiglu_qgemv(p, p, p, p, p, p, p, p, 0.0, p, 4, 64, None) == -1
+    for top_k in (0, 9):
+        assert q.lib.moe_qgemv_combine(p, p, p, p, p, p, 8, 64, 64, p, p, top_k, p, None, p,
+                                       p, None, None) == -1
+    assert q.lib.moe_qgemv_combine(p, p, p, p, p, p, 0, 64, 64, p, p, 4, p, None, p, p,
+                                   None, None) == -1
+    assert q.lib.decode_attention_seq1(p, p, 6, 4, 128, None) == -1
+
+
+def test_misaligned_status(q):
+    p, odd = _fake_ptr(), _fake_ptr(0x10001)
+    two = _fake_ptr(0x10002)
+    assert q.lib.qgemv_w4g64(two, p, p, p, p, 1, 4, 64, None, None) == -3   # codes need 4 B
+    assert q.lib.qgemv_w4g64(p, odd, p, p, p, 1, 4, 64, None, None) == -3
+    assert q.lib.qgemv_w4g64(p, p, p, p, p, 1, 4, 64, odd, None) == -3       # residual
+    assert q.lib.moe_qgemv_combine(p, p, p, p, p, p, 8, 64, 64, p, p, 4, p, None, p,
+                                   two, None, None) == -3                    # workspace
+
+
+def test_workspace_bytes_and_strerror(q):
+    assert q.moe_workspace_bytes(4, 1024) == 4 * 1024 * 4
+    assert q.moe_workspace_bytes(0, 1024) == 0
+    for s in (0, -1, -2, -3, -4, -5):
+        assert q.strerror(s) and q.strerror(s) != "unknown status"
+    assert q.strerror(-99) == "unknown status"
+
+
+def test_no_device_reports_edevice(q):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = _fake_ptr()
+    assert q.lib.qgemv_w4g64(p, p, p, p, p, 1, 4, 64, None, None) == -5
+
+
+def test_expert_byte_accounting_pins_group64_fp16():
+    """The hada.io page (topic 27758, "SSD Expert Streaming") gives about
+    6.75 MB per expert for hidden 4096 and 4-bit experts: 4096 x 2048 + 1024 x
+    4096 weights at 0.5625 B/weight is exactly 6.75 MiB."""
+    from bit_group_quantized_qgemv_gb300 import accounting as acc
+    assert acc.expert_bytes(4096, 1024, 4) == 7077888
+    assert acc.expert_bytes(4096, 1024, 4) == int(6.75 * 2**20)
+    # 8B layer total from the matvec shapes
+    assert sum(acc.weight_bytes(n, k, 4) for n, k in
+               [(6144, 4096), (4096, 4096), (2 * 14336, 4096), (4096, 14336)]) == 122683392
