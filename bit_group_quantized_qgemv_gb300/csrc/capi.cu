@@ -7,7 +7,7 @@
 
 #include <atomic>
 
-#include "../../include/qgemv.h"
+#include "qgemv.h"
 #include "qgemv_args.h"
 
 namespace {

@@ -18,9 +18,9 @@ enum Mode : int {
 };
 
 constexpr int kMaxStages = 16;
+constexpr int kSliceK = 32;  // k values of a row one streaming-kernel thread owns
 constexpr int kMaxTopK = 8;
 constexpr int kMaxM = 8;
-constexpr int kRedSlots = 128;  // JR * T / 32 <= 8 * 512 / 32
 
 struct StreamArgs {
   const uint8_t* codes[2];  // matrix 0 (or gate), matrix 1 (up); MoE: expert-0 bases
@@ -50,32 +50,23 @@ struct StreamArgs {
 struct StreamPlan {
   bool ok = false;
   int ub = 0, tg = 0, t = 0, s = 0, jr = 0, rs = 0, ns = 0, stage_bytes = 0, grid = 0;
+  int red_bytes = 0;   // partial-sum slots per stage
+  int x_bytes = 0;     // activations (fp16 pairs) and their unit sums
+  int smem_bytes = 0;  // dynamic shared memory: ns * (stage_bytes + red_bytes) + x_bytes
 };
 
-// Choose the unit size, thread counts, rows per stage and ring depth of the
-// streaming kernel.  ok = false when it does not apply (the generic kernel
-// runs instead): K must be a multiple of 1024 (2048 for 2-bit) so that each
-// task spans whole warps and every scale row is a multiple of 16 bytes.
+// Choose the thread counts, tasks per thread, rows per stage and ring depth
+// of the streaming kernel.  ok = false when it does not apply (the generic
+// kernel runs instead): K must be a multiple of 1024 and at most 16384, so
+// that a row's TG = K/32 slices span whole warps and every scale row is a
+// multiple of 16 bytes.
 inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, int top_k,
-                                   int sms, int target_threads = 256) {
+                                   int sms, int target_threads = 512, int max_jr = 4,
+                                   int stage_limit = 40 * 1024, int ring_budget = 200 * 1024) {
   StreamPlan p;
-  if (K % 1024 != 0 || rows <= 0 || sms <= 0) return p;
-  int tg = 0, ub = 0;
-  if (bits == 4) {
-    if ((K / 64) % 32 == 0 && K / 64 <= 512) {
-      ub = 32;
-      tg = K / 64;
-    } else if ((K / 32) % 32 == 0 && K / 32 <= 512) {
-      ub = 16;
-      tg = K / 32;
-    }
-  } else if (bits == 2) {
-    if ((K / 64) % 32 == 0 && K / 64 <= 512) {
-      ub = 16;
-      tg = K / 64;
-    }
-  }
-  if (tg == 0) return p;
+  if ((bits != 4 && bits != 2) || K % 1024 != 0 || K / kSliceK > 512 || rows <= 0 || sms <= 0)
+    return p;
+  const int tg = K / kSliceK;
   int s;
   if (mode == kMoeDown) {
     if (top_k < 1 || top_k > kMaxTopK || tg * top_k > 512) return p;
@@ -88,20 +79,24 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   }
   const int t = s * tg;
   if (t > 512) return p;
-  const int nmat = (mode == kSwiglu || mode == kMoeUp) ? 2 : (mode == kMoeDown ? top_k : 1);
-  const int rowstep = (mode == kMoeDown) ? s / top_k : s;
-  const int row_bytes = nmat * (K * bits / 8 + 2 * (K / 32));
-  int jr = 4;
-  if (static_cast<long long>(jr) * rowstep * row_bytes > 40 * 1024) jr = 2;
-  const int rs = jr * rowstep;
-  const long long stage = static_cast<long long>(rs) * row_bytes;
+  const int ms = (mode == kSwiglu || mode == kMoeUp) ? 2 : (mode == kMoeDown ? top_k : 1);
+  const int task_bytes = K * bits / 8 + 2 * (K / 32);  // one row of one matrix
+  int jr = max_jr;
+  while (jr > 1 && (static_cast<long long>(s) * jr * task_bytes > stage_limit || (s * jr) % ms))
+    jr /= 2;
+  if ((s * jr) % ms) return p;
+  const int tasks = s * jr;
+  const int rs = tasks / ms;
+  const long long stage = static_cast<long long>(tasks) * task_bytes;
   if (stage > 100 * 1024) return p;
-  int ns = static_cast<int>((200 * 1024) / stage);
+  const int red = ((tasks * (tg / 32) + 3) & ~3) * static_cast<int>(sizeof(float));
+  const int nvec = (mode == kMoeDown) ? top_k : 1;
+  const int xb = nvec * (K * 2 + (K / kSliceK) * static_cast<int>(sizeof(float)));
+  int ns = static_cast<int>((ring_budget - xb) / (stage + red));
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) return p;
-  if (jr * t / 32 > kRedSlots) return p;
   p.ok = true;
-  p.ub = ub;
+  p.ub = kSliceK * bits / 8;
   p.tg = tg;
   p.t = t;
   p.s = s;
@@ -109,6 +104,9 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   p.rs = rs;
   p.ns = ns;
   p.stage_bytes = static_cast<int>(stage);
+  p.red_bytes = red;
+  p.x_bytes = xb;
+  p.smem_bytes = ns * (static_cast<int>(stage) + red) + xb;
   p.grid = static_cast<int>(rows < sms ? rows : sms);
   return p;
 }

@@ -42,6 +42,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds; it
+// resumes as soon as the phase completes, so a waiting warp does not spin
+// through issue slots that computing warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -55,9 +69,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 127u) == 0u && global_timer_ns() - t0 > 1000000000ull) {
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (global_timer_ns() - t0 > 1000000000ull) {
       atomicOr(status, kStatusWaitTimeout);
       return false;
     }
@@ -118,13 +132,13 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 // fma(q, scale*x, bias*x) form of the FMA-reordered dequantisation,
 // factored over the 64 k of a group.
 //
-// xp[j] packs the activations (x_{8i+j}, x_{8i+j+4}) for j = 0..3.
-__device__ __forceinline__ void dot_word4(uint32_t w, uint32_t x0, uint32_t x1, uint32_t x2,
-                                          uint32_t x3, float& a, float& b) {
+// x[j] is the fp16 activation of k = 8i + j, one per 16-bit register, so no
+// instruction is spent taking halves of packed registers apart.
+__device__ __forceinline__ void dot_word4(uint32_t w, const unsigned short* x, float& a,
+                                          float& b) {
   asm("{\n"
       ".reg .b32 v0, v1, v2, v3, w8;\n"
       ".reg .b16 q0, q1, q2, q3, q4, q5, q6, q7;\n"
-      ".reg .b16 y0, y1, y2, y3, y4, y5, y6, y7;\n"
       "and.b32 v0, %2, 0x000F000F;\n"
       "and.b32 v1, %2, 0x00F000F0;\n"
       "shr.u32 w8, %2, 8;\n"
@@ -134,21 +148,18 @@ __device__ __forceinline__ void dot_word4(uint32_t w, uint32_t x0, uint32_t x1, 
       "mov.b32 {q1, q5}, v1;\n"
       "mov.b32 {q2, q6}, v2;\n"
       "mov.b32 {q3, q7}, v3;\n"
-      "mov.b32 {y0, y4}, %3;\n"
-      "mov.b32 {y1, y5}, %4;\n"
-      "mov.b32 {y2, y6}, %5;\n"
-      "mov.b32 {y3, y7}, %6;\n"
-      "fma.rn.f32.f16 %0, q0, y0, %0;\n"
-      "fma.rn.f32.f16 %1, q1, y1, %1;\n"
-      "fma.rn.f32.f16 %0, q4, y4, %0;\n"
-      "fma.rn.f32.f16 %1, q5, y5, %1;\n"
-      "fma.rn.f32.f16 %0, q2, y2, %0;\n"
-      "fma.rn.f32.f16 %1, q3, y3, %1;\n"
-      "fma.rn.f32.f16 %0, q6, y6, %0;\n"
-      "fma.rn.f32.f16 %1, q7, y7, %1;\n"
+      "fma.rn.f32.f16 %0, q0, %3, %0;\n"
+      "fma.rn.f32.f16 %1, q1, %4, %1;\n"
+      "fma.rn.f32.f16 %0, q4, %7, %0;\n"
+      "fma.rn.f32.f16 %1, q5, %8, %1;\n"
+      "fma.rn.f32.f16 %0, q2, %5, %0;\n"
+      "fma.rn.f32.f16 %1, q3, %6, %1;\n"
+      "fma.rn.f32.f16 %0, q6, %9, %0;\n"
+      "fma.rn.f32.f16 %1, q7, %10, %1;\n"
       "}"
       : "+f"(a), "+f"(b)
-      : "r"(w), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
+      : "r"(w), "h"(x[0]), "h"(x[1]), "h"(x[2]), "h"(x[3]), "h"(x[4]), "h"(x[5]), "h"(x[6]),
+        "h"(x[7]));
 }
 
 // A 2-bit word holds codes c_0..c_15 (k = 16i .. 16i+15), low bits first.
@@ -156,13 +167,12 @@ __device__ __forceinline__ void dot_word4(uint32_t w, uint32_t x0, uint32_t x1, 
 // the word >> 8) yield fp16 subnormals m * c * 2^-24 with m = 1, 4, 16, 64.
 // Class accumulators a (m=1), b (4), c (16), d (64):
 //   sum_k c_k x_k = (a + b / 4 + c / 16 + d / 64) * 2^24.
-// xp[j] packs (x_{16i+j}, x_{16i+j+8}) for j = 0..7.
-__device__ __forceinline__ void dot_word2(uint32_t w, const uint32_t* xp, float& a, float& b,
+// x[j] is the fp16 activation of k = 16i + j, one per 16-bit register.
+__device__ __forceinline__ void dot_word2(uint32_t w, const unsigned short* x, float& a, float& b,
                                           float& c, float& d) {
   asm("{\n"
       ".reg .b32 v0, v1, v2, v3, v4, v5, v6, v7, w8;\n"
       ".reg .b16 p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15;\n"
-      ".reg .b16 y0, y1, y2, y3, y4, y5, y6, y7, y8, y9, y10, y11, y12, y13, y14, y15;\n"
       "and.b32 v0, %4, 0x00030003;\n"
       "and.b32 v1, %4, 0x000C000C;\n"
       "and.b32 v2, %4, 0x00300030;\n"
@@ -180,34 +190,27 @@ __device__ __forceinline__ void dot_word2(uint32_t w, const uint32_t* xp, float&
       "mov.b32 {p5, p13}, v5;\n"
       "mov.b32 {p6, p14}, v6;\n"
       "mov.b32 {p7, p15}, v7;\n"
-      "mov.b32 {y0, y8}, %5;\n"
-      "mov.b32 {y1, y9}, %6;\n"
-      "mov.b32 {y2, y10}, %7;\n"
-      "mov.b32 {y3, y11}, %8;\n"
-      "mov.b32 {y4, y12}, %9;\n"
-      "mov.b32 {y5, y13}, %10;\n"
-      "mov.b32 {y6, y14}, %11;\n"
-      "mov.b32 {y7, y15}, %12;\n"
-      "fma.rn.f32.f16 %0, p0, y0, %0;\n"
-      "fma.rn.f32.f16 %1, p1, y1, %1;\n"
-      "fma.rn.f32.f16 %2, p2, y2, %2;\n"
-      "fma.rn.f32.f16 %3, p3, y3, %3;\n"
-      "fma.rn.f32.f16 %0, p8, y8, %0;\n"
-      "fma.rn.f32.f16 %1, p9, y9, %1;\n"
-      "fma.rn.f32.f16 %2, p10, y10, %2;\n"
-      "fma.rn.f32.f16 %3, p11, y11, %3;\n"
-      "fma.rn.f32.f16 %0, p4, y4, %0;\n"
-      "fma.rn.f32.f16 %1, p5, y5, %1;\n"
-      "fma.rn.f32.f16 %2, p6, y6, %2;\n"
-      "fma.rn.f32.f16 %3, p7, y7, %3;\n"
-      "fma.rn.f32.f16 %0, p12, y12, %0;\n"
-      "fma.rn.f32.f16 %1, p13, y13, %1;\n"
-      "fma.rn.f32.f16 %2, p14, y14, %2;\n"
-      "fma.rn.f32.f16 %3, p15, y15, %3;\n"
+      "fma.rn.f32.f16 %0, p0, %5, %0;\n"
+      "fma.rn.f32.f16 %1, p1, %6, %1;\n"
+      "fma.rn.f32.f16 %2, p2, %7, %2;\n"
+      "fma.rn.f32.f16 %3, p3, %8, %3;\n"
+      "fma.rn.f32.f16 %0, p8, %13, %0;\n"
+      "fma.rn.f32.f16 %1, p9, %14, %1;\n"
+      "fma.rn.f32.f16 %2, p10, %15, %2;\n"
+      "fma.rn.f32.f16 %3, p11, %16, %3;\n"
+      "fma.rn.f32.f16 %0, p4, %9, %0;\n"
+      "fma.rn.f32.f16 %1, p5, %10, %1;\n"
+      "fma.rn.f32.f16 %2, p6, %11, %2;\n"
+      "fma.rn.f32.f16 %3, p7, %12, %3;\n"
+      "fma.rn.f32.f16 %0, p12, %17, %0;\n"
+      "fma.rn.f32.f16 %1, p13, %18, %1;\n"
+      "fma.rn.f32.f16 %2, p14, %19, %2;\n"
+      "fma.rn.f32.f16 %3, p15, %20, %3;\n"
       "}"
       : "+f"(a), "+f"(b), "+f"(c), "+f"(d)
-      : "r"(w), "r"(xp[0]), "r"(xp[1]), "r"(xp[2]), "r"(xp[3]), "r"(xp[4]), "r"(xp[5]),
-        "r"(xp[6]), "r"(xp[7]));
+      : "r"(w), "h"(x[0]), "h"(x[1]), "h"(x[2]), "h"(x[3]), "h"(x[4]), "h"(x[5]), "h"(x[6]),
+        "h"(x[7]), "h"(x[8]), "h"(x[9]), "h"(x[10]), "h"(x[11]), "h"(x[12]), "h"(x[13]),
+        "h"(x[14]), "h"(x[15]));
 }
 
 // Code q of k within a packed word (generic path).

@@ -5,27 +5,37 @@
 //
 //  * Persistent: one CTA per SM.  CTA b owns the contiguous row range
 //    [b*R/P, (b+1)*R/P) of the R output rows (P CTAs), so every SM streams
-//    the same number of bytes and a CTA's codes, scales and biases are three
+//    the same number of bytes and a CTA's codes, scales and biases are
 //    contiguous blocks of memory.
 //  * Warp 0 (one lane) is the producer: it streams the range in stages of RS
-//    rows with 1-D TMA bulk copies (cp.async.bulk, L2 evict-first) into an
-//    NS-deep shared-memory ring guarded by mbarriers.  No multicast.
-//  * The other T threads are consumers.  Threads form tasks of TG threads;
-//    thread uu of a task owns the same 16- or 32-byte slice ("unit") of
-//    codes in every row, so its activations (32 or 64 fp16 values of x) sit
-//    in registers for the whole kernel, loaded once.  S = T / TG tasks run
-//    side by side; each thread handles JR rows of every stage.
+//    rows (of every matrix the op reads) with 1-D TMA bulk copies
+//    (cp.async.bulk, L2 evict-first) into an NS-deep shared-memory ring
+//    guarded by mbarriers.  No multicast.
+//  * The other T threads are consumers.  A stage holds MS x RS "tasks"
+//    (matrix slot, row).  Threads form slots of TG = K/32 threads; thread uu
+//    of a slot owns k in [32 uu, 32 uu + 32) of every row, so its 32
+//    activations sit in registers (one fp16 per register) for the whole
+//    kernel.  The S = T/TG slots take the tasks round-robin, JR per thread.
 //  * Inner loop: dot_word4 / dot_word2 (fp16-subnormal codes x fp16
 //    activations with the mixed fma.rn.f32.f16, exact products, fp32 sums),
-//    then scale * sum(q x) + bias * sum(x) per unit: the FMA-reordered
+//    then scale * sum(q x) + bias * sum(x) per slice: the FMA-reordered
 //    dequantisation of the hada.io page (topic 27758), factored per group.
-//  * Row sums: a warp transpose-reduce of the JR row partials (log2 JR
-//    split levels, then plain xor levels), one shared-memory slot per warp,
-//    a consumer-only named barrier, and TG/32 adds by the finaliser thread
-//    of each row, which applies the epilogue (residual, RMSNorm scale,
-//    SwiGLU, MoE weights) and stores.
+//  * Row sums: a warp transpose-reduce of the JR task partials (log2 JR
+//    split levels, then plain xor levels) and one shared-memory slot per
+//    warp and task.  Consumer warps never wait for each other: each stores
+//    its partials and arrives on the stage's "partials" mbarrier.  Warp 1
+//    is the epilogue warp: it waits for that barrier, sums the slots in a
+//    fixed order (deterministic), applies the epilogue (residual, RMSNorm
+//    scale, SwiGLU, MoE weights) and stores the rows.  A stage is released
+//    to the producer only when every consumer warp and the epilogue warp
+//    are done with it, so the slots are reused only after they were read.
+//  * The consumers' row loop is branch-free: all JR slices of a stage are
+//    computed (rows past the stage's end read stale but valid shared memory)
+//    and masked afterwards, so the compiler can interleave the rows' FMA
+//    chains and hoist their shared-memory loads.
 //  * Every mbarrier wait is bounded (about 1 s); a timeout sets a status bit
-//    and the kernel stops instead of hanging.
+//    and the waiting thread returns instead of hanging (no named barrier is
+//    entered after the first wait, so nothing is left waiting).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -38,30 +48,54 @@ namespace qgemv {
 // Status word of this translation unit (bit kStatusWaitTimeout).
 static __device__ unsigned g_status = 0;
 
-template <int BITS, int UB>
-struct Unit {
-  static constexpr int kWords = UB / 4;               // uint32 words per row slice
+template <int BITS>
+struct Slice {
   static constexpr int kCodesPerWord = 32 / BITS;
-  static constexpr int kK = kWords * kCodesPerWord;   // k values per slice
-  static constexpr int kPairs = kCodesPerWord / 2;    // packed x registers per word
-  static constexpr int kXRegs = kWords * kPairs;
+  static constexpr int kWords = kSliceK / kCodesPerWord;  // 4 (4-bit) or 2 (2-bit)
+  static constexpr int kBytes = kWords * 4;               // 16 or 8
 };
 
-// Rows in the stage that starts at `row`: up to RS, never past the CTA's
-// range, and (kMoeUp) never across an expert boundary.
-template <int MODE>
-__device__ __forceinline__ int stage_rows(long long row, long long r1, const StreamArgs& a) {
-  long long n = r1 - row;
-  if (n > a.RS) n = a.RS;
-  if (MODE == kMoeUp) {
-    const long long left = a.rows_per_expert - (row % a.rows_per_expert);
-    if (n > left) n = left;
-  }
-  return static_cast<int>(n);
-}
+// Stage walker shared by the producer and the consumers: the rows of each
+// stage (up to RS, never past the CTA's range and, for kMoeUp, never across
+// an expert boundary), the ring slot and its phase parity, all kept
+// incrementally (no divisions on the per-stage path).
+struct StageWalker {
+  int row, r1, rs, ns;
+  int rows_per_expert;  // kMoeUp only, else 0
+  int expert_slot, left_in_expert;
+  int slot;
+  uint32_t phase;
 
-// Transpose-reduce JR row partials across a warp.  Returns, on lanes with
-// lane % (32/JR) == 0, the warp's sum for row j = lane / (32/JR).
+  __device__ __forceinline__ StageWalker(int r0_, int r1_, int rs_, int ns_, int rpe)
+      : row(r0_), r1(r1_), rs(rs_), ns(ns_), rows_per_expert(rpe), slot(0), phase(0) {
+    expert_slot = rpe > 0 ? r0_ / rpe : 0;
+    left_in_expert = rpe > 0 ? rpe - (r0_ - expert_slot * rpe) : 0x7fffffff;
+  }
+  __device__ __forceinline__ bool more() const { return row < r1; }
+  __device__ __forceinline__ int rows() const {
+    int n = r1 - row;
+    if (n > rs) n = rs;
+    if (n > left_in_expert) n = left_in_expert;
+    return n;
+  }
+  __device__ __forceinline__ void advance(int n) {
+    row += n;
+    if (rows_per_expert > 0) {
+      left_in_expert -= n;
+      if (left_in_expert == 0) {
+        ++expert_slot;
+        left_in_expert = rows_per_expert;
+      }
+    }
+    if (++slot == ns) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Transpose-reduce JR partials across a warp.  Returns, on lanes with
+// lane % (32/JR) == 0, the warp's sum of partial j = lane / (32/JR).
 template <int JR>
 __device__ __forceinline__ float warp_reduce_rows(float (&v)[JR], int lane) {
 #pragma unroll
@@ -80,68 +114,48 @@ __device__ __forceinline__ float warp_reduce_rows(float (&v)[JR], int lane) {
   return r;
 }
 
-// Sum of the thread's x slice, pairwise in fp32 (error ~ log2(64) ulp).
-template <int N>
-__device__ __forceinline__ float pairwise_sum(float (&v)[N]) {
-#pragma unroll
-  for (int w = N / 2; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) v[i] += v[i + w];
-  return v[0];
-}
-
-// One row slice: sum over the unit of w * x, in units of 2^-24.
-template <int BITS, int UB>
-__device__ __forceinline__ float unit_dot(const uint8_t* codes, const uint32_t* xp, float s,
-                                          float b, float xs_scaled) {
-  using U = Unit<BITS, UB>;
-  uint32_t w[U::kWords];
-#pragma unroll
-  for (int i = 0; i < U::kWords / 4; ++i) {
-    const uint4 v = reinterpret_cast<const uint4*>(codes)[i];
-    w[4 * i + 0] = v.x;
-    w[4 * i + 1] = v.y;
-    w[4 * i + 2] = v.z;
-    w[4 * i + 3] = v.w;
-  }
+// One row slice: sum over its 32 k of w * x, in units of 2^-24.
+template <int BITS>
+__device__ __forceinline__ float slice_dot(const uint8_t* codes, const unsigned short* x, float s,
+                                           float b, float xs_scaled) {
   float t;
   if (BITS == 4) {
+    const uint4 c = *reinterpret_cast<const uint4*>(codes);
     float pa = 0.f, pb = 0.f, qa = 0.f, qb = 0.f;
-#pragma unroll
-    for (int i = 0; i < U::kWords; i += 2) {
-      dot_word4(w[i], xp[4 * i], xp[4 * i + 1], xp[4 * i + 2], xp[4 * i + 3], pa, pb);
-      if (i + 1 < U::kWords)
-        dot_word4(w[i + 1], xp[4 * i + 4], xp[4 * i + 5], xp[4 * i + 6], xp[4 * i + 7], qa, qb);
-    }
+    dot_word4(c.x, x + 0, pa, pb);
+    dot_word4(c.y, x + 8, qa, qb);
+    dot_word4(c.z, x + 16, pa, pb);
+    dot_word4(c.w, x + 24, qa, qb);
     t = fmaf(pb + qb, 0.0625f, pa + qa);
   } else {
+    const uint2 c = *reinterpret_cast<const uint2*>(codes);
     float ca = 0.f, cb = 0.f, cc = 0.f, cd = 0.f;
-#pragma unroll
-    for (int i = 0; i < U::kWords; ++i) dot_word2(w[i], xp + 8 * i, ca, cb, cc, cd);
+    dot_word2(c.x, x + 0, ca, cb, cc, cd);
+    dot_word2(c.y, x + 16, ca, cb, cc, cd);
     t = fmaf(cd, 0.015625f, fmaf(cc, 0.0625f, fmaf(cb, 0.25f, ca)));
   }
   return fmaf(s, t, b * xs_scaled);
 }
 
-template <int BITS, int UB, int MODE, int JR>
-__global__ void __launch_bounds__(544, 1) stream_kernel(const StreamArgs a) {
-  using U = Unit<BITS, UB>;
+template <int BITS, int MODE, int JR>
+__global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
+  using SL = Slice<BITS>;
   constexpr int NMAT = (MODE == kSwiglu || MODE == kMoeUp) ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ float red[2][NMAT][kRedSlots];
+  __shared__ __align__(8) uint64_t part_bar[kMaxStages];
   __shared__ float s_norm[17];
   __shared__ int s_eidx[kMaxTopK];
   __shared__ float s_ewt[kMaxTopK];
-  __shared__ int s_abort;
 
-  const int T = static_cast<int>(blockDim.x) - 32;
+  const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int NS = a.NS;
-  const long long r0 = static_cast<long long>(blockIdx.x) * a.rows / gridDim.x;
-  const long long r1 = static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x;
+  const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
+  const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
+  const int rpe = (MODE == kMoeUp) ? a.rows_per_expert : 0;
   const int rcb = a.K * BITS / 8;  // code bytes per row
   const int rgb = a.K / 32;        // scale (or bias) bytes per row
   const int MS = (MODE == kMoeDown) ? a.top_k : NMAT;  // matrices per stage
@@ -150,10 +164,10 @@ __global__ void __launch_bounds__(544, 1) stream_kernel(const StreamArgs a) {
   const int biases_off = scales_off + MS * a.RS * rgb;
 
   if (threadIdx.x == 0) {
-    s_abort = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32));
+      mbar_init(smem_u32(&part_bar[s]), static_cast<uint32_t>(T / 32));
+      mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32 + 1));
     }
     fence_mbar_init();
     if (MODE == kMoeUp || MODE == kMoeDown) {
@@ -172,53 +186,46 @@ __global__ void __launch_bounds__(544, 1) stream_kernel(const StreamArgs a) {
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int it = 0;
-      for (long long row = r0; row < r1; ++it) {
-        const int n = stage_rows<MODE>(row, r1, a);
-        const int s = it % NS;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ((it / NS) & 1) ^ 1, &g_status)) break;
+      int issued = 0;
+      for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+        const int n = wk.rows();
+        const int s = wk.slot;
+        if (!mbar_wait(smem_u32(&empty_bar[s]), wk.phase ^ 1u, &g_status)) break;
         const uint32_t fb = smem_u32(&full_bar[s]);
         const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * a.stage_bytes);
-        // Sources of each matrix slot for rows [row, row + n).
-        const uint8_t* cs[kMaxTopK];
-        const __half* ss[kMaxTopK];
-        const __half* bs[kMaxTopK];
+        // Expected bytes of every valid matrix slot first, then the copies.
         uint32_t bytes = 0;
         for (int m = 0; m < MS; ++m) {
-          long long lrow = row;
-          long long ec = 0, eg = 0;
-          const int which = (MODE == kMoeDown) ? 0 : m;
-          bool valid = true;
-          if (MODE == kMoeUp) {
-            const int e = s_eidx[row / a.rows_per_expert];
-            valid = e >= 0;
-            lrow = row % a.rows_per_expert;
-            ec = static_cast<long long>(e) * a.ex_code_bytes;
-            eg = static_cast<long long>(e) * a.ex_groups;
-          } else if (MODE == kMoeDown) {
-            const int e = s_eidx[m];
-            valid = e >= 0;
-            ec = static_cast<long long>(e) * a.ex_code_bytes;
-            eg = static_cast<long long>(e) * a.ex_groups;
-          }
-          if (!valid) {
-            cs[m] = nullptr;
-            continue;
-          }
-          cs[m] = a.codes[which] + ec + lrow * rcb;
-          ss[m] = a.scales[which] + eg + lrow * (rgb / 2);
-          bs[m] = a.biases[which] + eg + lrow * (rgb / 2);
-          bytes += static_cast<uint32_t>(n) * static_cast<uint32_t>(rcb + 2 * rgb);
+          const int e = (MODE == kMoeUp)     ? s_eidx[wk.expert_slot]
+                        : (MODE == kMoeDown) ? s_eidx[m]
+                                             : 0;
+          if (e >= 0) bytes += static_cast<uint32_t>(n) * static_cast<uint32_t>(rcb + 2 * rgb);
         }
         mbar_arrive_expect_tx(fb, bytes);
         for (int m = 0; m < MS; ++m) {
-          if (cs[m] == nullptr) continue;
-          bulk_g2s(st + codes_off + m * a.RS * rcb, cs[m], n * rcb, fb, pol);
-          bulk_g2s(st + scales_off + m * a.RS * rgb, ss[m], n * rgb, fb, pol);
-          bulk_g2s(st + biases_off + m * a.RS * rgb, bs[m], n * rgb, fb, pol);
+          long long lrow = wk.row;
+          int e = 0;
+          if (MODE == kMoeUp) {
+            e = s_eidx[wk.expert_slot];
+            lrow = rpe - wk.left_in_expert;
+          } else if (MODE == kMoeDown) {
+            e = s_eidx[m];
+          }
+          if (e < 0) continue;
+          const int which = (MODE == kMoeDown) ? 0 : m;
+          const long long ec = static_cast<long long>(e) * a.ex_code_bytes;
+          const long long eg = static_cast<long long>(e) * a.ex_groups;
+          bulk_g2s(st + codes_off + m * a.RS * rcb, a.codes[which] + ec + lrow * rcb, n * rcb, fb,
+                   pol);
+          bulk_g2s(st + scales_off + m * a.RS * rgb, a.scales[which] + eg + lrow * (rgb / 2),
+                   n * rgb, fb, pol);
+          bulk_g2s(st + biases_off + m * a.RS * rgb, a.biases[which] + eg + lrow * (rgb / 2),
+                   n * rgb, fb, pol);
         }
-        row += n;
+        ++issued;
+        wk.advance(n);
       }
+      const int it = issued;
       // Drain: never leave while a copy into this CTA's shared memory is in flight.
       for (int j = (it > NS ? it - NS : 0); j < it; ++j)
         mbar_wait(smem_u32(&full_bar[j % NS]), (j / NS) & 1, &g_status);
@@ -226,196 +233,216 @@ __global__ void __launch_bounds__(544, 1) stream_kernel(const StreamArgs a) {
     return;
   }
 
-  // ------------------------------------------------------------ consumers
-  const int t = threadIdx.x - 32;
+  // ------------------------------------------------- consumers and epilogue
+  const bool epi = (warp == 1);           // the epilogue warp
+  const int t = threadIdx.x - 64;         // consumer index (negative for warp 1)
   const int TG = a.TG;
   const int S = a.S;
-  const int slot = t / TG;
-  const int uu = t - slot * TG;  // this thread's unit (row slice) index
-  const int wit = uu >> 5;       // warp index within the task
-  const int wpt = TG >> 5;       // warps per task
-  int ek = 0, rbase = slot, rstep = S;
-  if (MODE == kMoeDown) {
-    ek = slot % a.top_k;
-    rbase = slot / a.top_k;
-    rstep = S / a.top_k;
-  }
+  const int slot = epi ? 0 : t / TG;
+  const int uu = epi ? 0 : t - slot * TG;  // this thread's slice index within a row
+  const int wit = uu >> 5;       // warp index within the slot
+  const int wpt = TG >> 5;       // warps per slot
+  const int ek = (MODE == kMoeDown) ? slot % a.top_k : 0;  // kMoeDown: fixed expert slot
   const bool use_gamma = (MODE == kNorm) || (MODE == kSwiglu && a.gamma != nullptr);
+  const int nwarps = T / 32;
+  const int tasks = MS * a.RS;  // per stage
+  // Per-stage partial-sum slots, after the ring: [NS][tasks][wpt].
+  float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(NS) * a.stage_bytes);
+  const int red_stage = (tasks * wpt + 3) & ~3;  // floats, 16-byte multiple
 
-  // RMS of x (kNorm, kSwiglu with gamma): every consumer sums a strided part.
-  float rstd = 1.f;
-  if (use_gamma) {
-    float ss = 0.f;
-    for (int k = t; k < a.K; k += T) {
-      const float v = __half2float(a.x[k]);
-      ss = fmaf(v, v, ss);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s_norm[warp - 1] = ss;
-    named_bar_sync(1, T);
-    if (t == 0) {
-      float tot = 0.f;
-      for (int w = 0; w < T / 32; ++w) tot += s_norm[w];
-      s_norm[16] = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
-    }
-    named_bar_sync(1, T);
-    rstd = s_norm[16];
-  }
-
-  // This thread's activations, packed in the pairing the dot routines use,
-  // and their sum (times 2^-24, the dot products' scale).
-  uint32_t xp[U::kXRegs];
-  float xs_scaled;
-  {
-    const int k0 = uu * U::kK;
-    float xv[U::kK];
+  // Activations, converted once per CTA into shared memory (after the ring
+  // and the partial-sum slots): fp16 in k order, and the fp32 sum of every
+  // 32-k slice.  kMoeDown keeps one vector per expert slot.
+  const int nvec = (MODE == kMoeDown) ? a.top_k : 1;
+  const int spv = a.K / kSliceK;  // slices per vector
+  __half* x_sm = reinterpret_cast<__half*>(red + static_cast<size_t>(NS) * red_stage);
+  float* xsum_sm = reinterpret_cast<float*>(x_sm + static_cast<size_t>(nvec) * a.K);
+  float sq = 0.f;
+  // One group of 8 activations per thread and trip; 4 lanes make a slice.
+  for (int gi = t; !epi && gi < nvec * a.K / 8; gi += T) {  // lane-uniform trip count
+    const int v = gi / (a.K / 8);
+    const int k0 = (gi - v * (a.K / 8)) * 8;
+    float xv[8];
     if (MODE == kMoeDown) {
-      const float4* src = reinterpret_cast<const float4*>(a.xf + static_cast<size_t>(ek) * a.K + k0);
-#pragma unroll
-      for (int i = 0; i < U::kK / 4; ++i) {
-        const float4 v = src[i];
-        xv[4 * i + 0] = v.x;
-        xv[4 * i + 1] = v.y;
-        xv[4 * i + 2] = v.z;
-        xv[4 * i + 3] = v.w;
-      }
+      const float4* src = reinterpret_cast<const float4*>(a.xf + static_cast<size_t>(v) * a.K + k0);
+      const float4 f0 = src[0], f1 = src[1];
+      xv[0] = f0.x;
+      xv[1] = f0.y;
+      xv[2] = f0.z;
+      xv[3] = f0.w;
+      xv[4] = f1.x;
+      xv[5] = f1.y;
+      xv[6] = f1.z;
+      xv[7] = f1.w;
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + k0);
+      const uint4 raw = *reinterpret_cast<const uint4*>(a.x + k0);
+      const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-      for (int i = 0; i < U::kK / 8; ++i) {
-        const uint4 v = src[i];
-        const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(h[j]);
-          xv[8 * i + 2 * j] = f.x;
-          xv[8 * i + 2 * j + 1] = f.y;
-        }
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(h[j]);
+        xv[2 * j] = f.x;
+        xv[2 * j + 1] = f.y;
+        sq = fmaf(f.x, f.x, fmaf(f.y, f.y, sq));
       }
       if (use_gamma) {
-        const uint4* gsrc = reinterpret_cast<const uint4*>(a.gamma + k0);
+        const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + k0);
+        const __half2* g = reinterpret_cast<const __half2*>(&graw);
 #pragma unroll
-        for (int i = 0; i < U::kK / 8; ++i) {
-          const uint4 v = gsrc[i];
-          const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(h[j]);
-            xv[8 * i + 2 * j] *= f.x;
-            xv[8 * i + 2 * j + 1] *= f.y;
-          }
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(g[j]);
+          xv[2 * j] *= f.x;
+          xv[2 * j + 1] *= f.y;
         }
       }
     }
     // Round to fp16 once (the kernel multiplies fp16 activations).
-    __half xh[U::kK];
+    uint4 packed;
+    uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
+    float part = 0.f;
 #pragma unroll
-    for (int k = 0; k < U::kK; ++k) {
-      xh[k] = __float2half_rn(xv[k]);
-      xv[k] = __half2float(xh[k]);
+    for (int j = 0; j < 4; ++j) {
+      const __half lo = __float2half_rn(xv[2 * j]), hi = __float2half_rn(xv[2 * j + 1]);
+      pw[j] = pack_half2(lo, hi);
+      part += __half2float(lo) + __half2float(hi);
     }
-    constexpr int cpw = U::kCodesPerWord;
-#pragma unroll
-    for (int i = 0; i < U::kWords; ++i)
-#pragma unroll
-      for (int j = 0; j < U::kPairs; ++j)
-        xp[i * U::kPairs + j] = pack_half2(xh[i * cpw + j], xh[i * cpw + j + cpw / 2]);
-    xs_scaled = pairwise_sum(xv) * kTwoM24;
+    *reinterpret_cast<uint4*>(x_sm + static_cast<size_t>(gi) * 8) = packed;
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    if ((lane & 3) == 0) xsum_sm[gi / 4] = part;
   }
-  const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
-  const int group_in_row = (uu * U::kK) / 64;
-
-  // `alive` turns false for good once a wait has run out (here or in a
-  // sibling warp, seen through s_abort after a barrier).  Every consumer then
-  // keeps walking the same stages and barriers without waiting or working,
-  // so no thread is ever left alone at a named barrier.
-  bool alive = true;
-  int it = 0, buf = 0;
-  for (long long row = r0; row < r1; ++it) {
-    const int n = stage_rows<MODE>(row, r1, a);
-    const int s = it % NS;
-    if (alive && __any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_abort) != 0))
-      alive = false;
-    if (alive) {
-      const bool got = mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, &g_status);
-      alive = __all_sync(0xffffffffu, got);
-      if (!alive && lane == 0) *reinterpret_cast<volatile int*>(&s_abort) = 1;
+  float rstd = 1.f;
+  if (use_gamma && !epi) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) s_norm[warp - 2] = sq;
+  }
+  // The only barrier among consumers and the epilogue warp; it runs before
+  // any mbarrier wait.
+  named_bar_sync(1, T + 32);
+  if (use_gamma) {
+    float tot = 0.f;
+    for (int w = 0; w < nwarps; ++w) tot += s_norm[w];
+    rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+  }
+  if (epi) {
+    // Epilogue warp: finish every stage's rows once all partials are in.
+    for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+      const int n = wk.rows();
+      const int s = wk.slot;
+      const int row = wk.row;
+      if (!mbar_wait(smem_u32(&part_bar[s]), wk.phase, &g_status)) return;
+      const bool ok = (MODE == kMoeUp) ? (s_eidx[wk.expert_slot] >= 0) : true;
+      const float* rs = red + static_cast<size_t>(s) * red_stage;
+      for (int r = lane; r < n; r += 32) {
+        const int gr = row + r;
+        float v[NMAT];
+        if (MODE == kMoeDown) {
+          v[0] = 0.f;
+          for (int k = 0; k < a.top_k; ++k) {
+            float e = 0.f;
+            for (int w = 0; w < wpt; ++w) e += rs[(r * a.top_k + k) * wpt + w];
+            v[0] = fmaf(s_ewt[k], e, v[0]);
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+            v[m] = 0.f;
+            for (int w = 0; w < wpt; ++w) v[m] += rs[(m * a.RS + r) * wpt + w];
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) v[m] *= kTwo24;
+        if (MODE == kPlain || MODE == kMoeDown) {
+          float o = v[0];
+          if (a.residual != nullptr) o += __half2float(a.residual[gr]);
+          a.y[gr] = __float2half_rn(o);
+        } else if (MODE == kNorm) {
+          a.y[gr] = __float2half_rn(v[0] * rstd);
+        } else if (MODE == kSwiglu) {
+          const float g = v[0] * rstd, u = v[NMAT - 1] * rstd;
+          a.y[gr] = __float2half_rn(silu_f(g) * u);
+        } else if (MODE == kMoeUp) {
+          a.yf[gr] = ok ? silu_f(v[0]) * v[NMAT - 1] : 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+      wk.advance(n);
     }
+    return;
+  }
+
+  // This thread's 32 activations, one fp16 per register, and their sum
+  // (times 2^-24, the dot products' scale).
+  unsigned short xr[kSliceK];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(x_sm + static_cast<size_t>(ek) * a.K +
+                                                      static_cast<size_t>(uu) * kSliceK);
+#pragma unroll
+    for (int i = 0; i < kSliceK / 8; ++i) {
+      const uint4 v = src[i];
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xr[8 * i + 2 * j] = static_cast<unsigned short>(w4[j] & 0xffffu);
+        xr[8 * i + 2 * j + 1] = static_cast<unsigned short>(w4[j] >> 16);
+      }
+    }
+  }
+  const float xs_scaled = xsum_sm[ek * spv + uu] * kTwoM24;
+  const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
+  const int group_in_row = (uu * kSliceK) / 64;
+  // Task j of this thread in every stage: matrix slot and row, and the
+  // shared-memory offsets of its slice.
+  int task_row[JR], code_off[JR], group_off[JR];
+#pragma unroll
+  for (int j = 0; j < JR; ++j) {
+    const int task = slot + j * S;
+    int ms, rl;
+    if (MODE == kMoeDown) {
+      ms = ek;
+      rl = task / a.top_k;
+    } else {
+      ms = task / a.RS;
+      rl = task - ms * a.RS;
+    }
+    task_row[j] = rl;
+    code_off[j] = (ms * a.RS + rl) * rcb + uu * SL::kBytes;
+    group_off[j] = (ms * a.RS + rl) * rgb + group_in_row * 2;
+  }
+
+  for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+    const int n = wk.rows();
+    const int s = wk.slot;
+    const int row = wk.row;
+    if (!mbar_wait(smem_u32(&full_bar[s]), wk.phase, &g_status)) return;
     const uint8_t* st = smem + static_cast<size_t>(s) * a.stage_bytes;
     bool slot_ok = expert_ok;
-    if (MODE == kMoeUp) slot_ok = s_eidx[row / a.rows_per_expert] >= 0;
-    const bool work = alive && slot_ok;
+    if (MODE == kMoeUp) slot_ok = s_eidx[wk.expert_slot] >= 0;
 
-    float acc[NMAT][JR];
+    float acc[JR];
 #pragma unroll
     for (int j = 0; j < JR; ++j) {
-      const int rl = rbase + j * rstep;
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        acc[m][j] = 0.f;
-        if (rl < n && work) {
-          const int ms = (MODE == kMoeDown) ? ek : m;
-          const uint8_t* cp = st + codes_off + (ms * a.RS + rl) * rcb + uu * UB;
-          const __half* sp =
-              reinterpret_cast<const __half*>(st + scales_off + (ms * a.RS + rl) * rgb);
-          const __half* bp =
-              reinterpret_cast<const __half*>(st + biases_off + (ms * a.RS + rl) * rgb);
-          acc[m][j] = unit_dot<BITS, UB>(cp, xp, __half2float(sp[group_in_row]),
-                                         __half2float(bp[group_in_row]), xs_scaled);
-        }
-      }
+      const __half sv = *reinterpret_cast<const __half*>(st + scales_off + group_off[j]);
+      const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
+      const float v = slice_dot<BITS>(st + codes_off + code_off[j], xr, __half2float(sv),
+                                      __half2float(bv), xs_scaled);
+      acc[j] = (task_row[j] < n && slot_ok) ? v : 0.f;
+    }
+
+    // Warp partials of this stage's tasks into the stage's slots.
+    float* rs = red + static_cast<size_t>(s) * red_stage;
+    {
+      constexpr int kLanesPerRow = 32 / JR;
+      const float v = warp_reduce_rows<JR>(acc, lane);
+      if ((lane & (kLanesPerRow - 1)) == 0) rs[(slot + (lane / kLanesPerRow) * S) * wpt + wit] = v;
     }
     __syncwarp();
-    if (lane == 0 && alive) mbar_arrive(smem_u32(&empty_bar[s]));
-
-    constexpr int kLanesPerRow = 32 / JR;
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      const float v = warp_reduce_rows<JR>(acc[m], lane);
-      if ((lane & (kLanesPerRow - 1)) == 0) {
-        const int j = lane / kLanesPerRow;
-        const int rl = rbase + j * rstep;
-        const int task = (MODE == kMoeDown) ? rl * a.top_k + ek : rl;
-        red[buf][m][task * wpt + wit] = v;
-      }
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&part_bar[s]));
+      mbar_arrive(smem_u32(&empty_bar[s]));
     }
-    named_bar_sync(1, T);
-
-    if (t < n && alive) {
-      const long long gr = row + t;
-      float v[NMAT];
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) v[m] = 0.f;
-      if (MODE == kMoeDown) {
-        for (int k = 0; k < a.top_k; ++k) {
-          float e = 0.f;
-          for (int w = 0; w < wpt; ++w) e += red[buf][0][(t * a.top_k + k) * wpt + w];
-          v[0] = fmaf(s_ewt[k], e, v[0]);
-        }
-      } else {
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-          for (int w = 0; w < wpt; ++w) v[m] += red[buf][m][t * wpt + w];
-      }
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) v[m] *= kTwo24;
-
-      if (MODE == kPlain || MODE == kMoeDown) {
-        float o = v[0];
-        if (a.residual != nullptr) o += __half2float(a.residual[gr]);
-        a.y[gr] = __float2half_rn(o);
-      } else if (MODE == kNorm) {
-        a.y[gr] = __float2half_rn(v[0] * rstd);
-      } else if (MODE == kSwiglu) {
-        const float g = v[0] * rstd, u = v[NMAT - 1] * rstd;
-        a.y[gr] = __float2half_rn(silu_f(g) * u);
-      } else if (MODE == kMoeUp) {
-        a.yf[gr] = slot_ok ? silu_f(v[0]) * v[NMAT - 1] : 0.f;
-      }
-    }
-    buf ^= 1;
-    row += n;
+    wk.advance(n);
   }
 }
 
@@ -430,12 +457,11 @@ inline cudaError_t ensure_smem_attr(F* kernel, int bytes, unsigned* done_mask, i
   return e;
 }
 
-template <int BITS, int UB, int MODE, int JR>
+template <int BITS, int MODE, int JR>
 inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream_t stream,
                                    int device) {
   static unsigned done_mask = 0;
-  auto* k = stream_kernel<BITS, UB, MODE, JR>;
-  const int dyn = p.ns * p.stage_bytes;
+  auto* k = stream_kernel<BITS, MODE, JR>;
   cudaError_t e = ensure_smem_attr(k, 220 * 1024, &done_mask, device);
   if (e != cudaSuccess) return e;
   a.TG = p.tg;
@@ -443,21 +469,20 @@ inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream
   a.RS = p.rs;
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
-  k<<<p.grid, p.t + 32, dyn, stream>>>(a);
+  k<<<p.grid, p.t + 64, p.smem_bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
-// Dispatch on the plan's unit size and rows per thread.
+// Dispatch on the plan's tasks per thread.
 template <int BITS, int MODE>
 inline cudaError_t launch_stream(const StreamPlan& p, const StreamArgs& a, cudaStream_t stream,
                                  int device) {
-  if constexpr (BITS == 4) {
-    if (p.ub == 32)
-      return p.jr == 4 ? launch_stream_t<BITS, 32, MODE, 4>(p, a, stream, device)
-                       : launch_stream_t<BITS, 32, MODE, 2>(p, a, stream, device);
+  switch (p.jr) {
+    case 8: return launch_stream_t<BITS, MODE, 8>(p, a, stream, device);
+    case 4: return launch_stream_t<BITS, MODE, 4>(p, a, stream, device);
+    case 2: return launch_stream_t<BITS, MODE, 2>(p, a, stream, device);
+    default: return launch_stream_t<BITS, MODE, 1>(p, a, stream, device);
   }
-  return p.jr == 4 ? launch_stream_t<BITS, 16, MODE, 4>(p, a, stream, device)
-                   : launch_stream_t<BITS, 16, MODE, 2>(p, a, stream, device);
 }
 
 // Read and clear this translation unit's status word (synchronous).
