@@ -45,6 +45,7 @@ struct StreamArgs {
   int M;                    // batch (generic kPlain only; 1 elsewhere)
   int TG, S, RS, NS;        // launch plan of the streaming kernel
   int stage_bytes;
+  int interleave;           // 1: CTAs take stages round-robin (see StageWalker)
 };
 
 struct StreamPlan {
@@ -52,6 +53,7 @@ struct StreamPlan {
   int ub = 0, tg = 0, t = 0, s = 0, jr = 0, rs = 0, ns = 0, stage_bytes = 0, grid = 0;
   int red_bytes = 0;   // partial-sum slots per stage
   int x_bytes = 0;     // activations (fp16 pairs) and their unit sums
+  int interleave = 0;  // 1: CTAs take stages round-robin
   int smem_bytes = 0;  // dynamic shared memory: ns * (stage_bytes + red_bytes) + x_bytes
 };
 
@@ -62,7 +64,8 @@ struct StreamPlan {
 // multiple of 16 bytes.
 inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, int top_k,
                                    int sms, int target_threads = 512, int max_jr = 4,
-                                   int stage_limit = 40 * 1024, int ring_budget = 200 * 1024) {
+                                   int stage_limit = 40 * 1024, int ring_budget = 200 * 1024,
+                                   bool interleave_ok = true) {
   StreamPlan p;
   if ((bits != 4 && bits != 2) || K % 1024 != 0 || K / kSliceK > 512 || rows <= 0 || sms <= 0)
     return p;
@@ -108,6 +111,14 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   p.x_bytes = xb;
   p.smem_bytes = ns * (static_cast<int>(stage) + red) + xb;
   p.grid = static_cast<int>(rows < sms ? rows : sms);
+  // Interleave stages across CTAs when that keeps the SMs within one stage
+  // of each other (and, for kMoeUp, stages never straddle experts).
+  const long long stages = (rows + rs - 1) / rs;
+  const bool experts_align = (mode != kMoeUp) || ((rows / (top_k > 0 ? top_k : 1)) % rs == 0);
+  if (interleave_ok && experts_align && stages >= 4LL * sms) {
+    p.interleave = 1;
+    p.grid = sms;
+  }
   return p;
 }
 

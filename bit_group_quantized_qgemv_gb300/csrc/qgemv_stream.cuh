@@ -55,19 +55,27 @@ struct Slice {
   static constexpr int kBytes = kWords * 4;               // 16 or 8
 };
 
-// Stage walker shared by the producer and the consumers: the rows of each
-// stage (up to RS, never past the CTA's range and, for kMoeUp, never across
-// an expert boundary), the ring slot and its phase parity, all kept
-// incrementally (no divisions on the per-stage path).
+// Stage walker shared by the producer, the consumers and the epilogue warp:
+// the rows of each stage, the ring slot and its phase parity.
+//  * contiguous (stride == 0): the CTA walks its own row range [r0, r1) in
+//    stages of up to RS rows (for kMoeUp never across an expert boundary);
+//  * interleaved (stride > 0): stage g covers rows [g RS, g RS + RS) and the
+//    CTA walks g = blockIdx.x, + P, + 2P, ..., so at any moment all SMs read
+//    neighbouring stages of the same region of memory.  (Used when every
+//    expert boundary falls on a stage boundary.)
+// No divisions on the per-stage path except kMoeUp's interleaved expert
+// lookup.
 struct StageWalker {
   int row, r1, rs, ns;
   int rows_per_expert;  // kMoeUp only, else 0
   int expert_slot, left_in_expert;
+  int stride;           // rows between this CTA's stages when interleaved, else 0
   int slot;
   uint32_t phase;
 
-  __device__ __forceinline__ StageWalker(int r0_, int r1_, int rs_, int ns_, int rpe)
-      : row(r0_), r1(r1_), rs(rs_), ns(ns_), rows_per_expert(rpe), slot(0), phase(0) {
+  __device__ __forceinline__ StageWalker(int r0_, int r1_, int rs_, int ns_, int rpe, int stride_)
+      : row(r0_), r1(r1_), rs(rs_), ns(ns_), rows_per_expert(rpe), stride(stride_), slot(0),
+        phase(0) {
     expert_slot = rpe > 0 ? r0_ / rpe : 0;
     left_in_expert = rpe > 0 ? rpe - (r0_ - expert_slot * rpe) : 0x7fffffff;
   }
@@ -79,12 +87,20 @@ struct StageWalker {
     return n;
   }
   __device__ __forceinline__ void advance(int n) {
-    row += n;
-    if (rows_per_expert > 0) {
-      left_in_expert -= n;
-      if (left_in_expert == 0) {
-        ++expert_slot;
-        left_in_expert = rows_per_expert;
+    if (stride > 0) {
+      row += stride;
+      if (rows_per_expert > 0 && row < r1) {
+        expert_slot = row / rows_per_expert;
+        left_in_expert = rows_per_expert - (row - expert_slot * rows_per_expert);
+      }
+    } else {
+      row += n;
+      if (rows_per_expert > 0) {
+        left_in_expert -= n;
+        if (left_in_expert == 0) {
+          ++expert_slot;
+          left_in_expert = rows_per_expert;
+        }
       }
     }
     if (++slot == ns) {
@@ -153,8 +169,13 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int NS = a.NS;
-  const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
-  const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
+  const int stride = a.interleave ? static_cast<int>(gridDim.x) * a.RS : 0;
+  const int r0 = a.interleave
+                     ? static_cast<int>(blockIdx.x) * a.RS
+                     : static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
+  const int r1 = a.interleave
+                     ? static_cast<int>(a.rows)
+                     : static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
   const int rpe = (MODE == kMoeUp) ? a.rows_per_expert : 0;
   const int rcb = a.K * BITS / 8;  // code bytes per row
   const int rgb = a.K / 32;        // scale (or bias) bytes per row
@@ -187,7 +208,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       int issued = 0;
-      for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+      for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
         const int n = wk.rows();
         const int s = wk.slot;
         if (!mbar_wait(smem_u32(&empty_bar[s]), wk.phase ^ 1u, &g_status)) break;
@@ -326,7 +347,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   }
   if (epi) {
     // Epilogue warp: finish every stage's rows once all partials are in.
-    for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+    for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
       const int n = wk.rows();
       const int s = wk.slot;
       const int row = wk.row;
@@ -411,7 +432,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     group_off[j] = (ms * a.RS + rl) * rgb + group_in_row * 2;
   }
 
-  for (StageWalker wk(r0, r1, a.RS, NS, rpe); wk.more();) {
+  for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
     const int n = wk.rows();
     const int s = wk.slot;
     const int row = wk.row;
@@ -469,6 +490,7 @@ inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream
   a.RS = p.rs;
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
+  a.interleave = p.interleave;
   k<<<p.grid, p.t + 64, p.smem_bytes, stream>>>(a);
   return cudaGetLastError();
 }
