@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     last_cuda_error,
     lib,
     moe_qgemv_combine,
+    moe_qgemv_combine_noalloc,
+    noalloc_max_scratch_bytes,
     moe_workspace_bytes,
     qgemv_w2g64,
     qgemv_w4g64,

@@ -27,6 +27,9 @@ _SIGS = {
     "moe_qgemv_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
                                _P, _P, _P, _P]),
     "qgemv_moe_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
+    "moe_qgemv_combine_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
+                                       _P, _P, _P]),
+    "qgemv_noalloc_max_scratch": (ctypes.c_size_t, []),
     "decode_attention_seq1": (_I, [_P, _P, _I, _I, _I, _P]),
     "qgemv_strerror": (ctypes.c_char_p, [_I]),
     "qgemv_last_cuda_error": (_I, []),
@@ -183,6 +186,33 @@ def moe_qgemv_combine(gu, dn, expert_idx, expert_w, x, residual=None, y=None, wo
                                _stream(stream))
     _check(st, "moe_qgemv_combine")
     return y
+
+
+def moe_qgemv_combine_noalloc(gu, dn, expert_idx, expert_w, x, residual=None, y=None,
+                              err_flag=None, stream=None):
+    """moe_qgemv_combine without a workspace: the library's fixed scratch array
+    stands in for it (see include/qgemv.h for its size limit and sharing)."""
+    gc, gs, gb = _weight(gu, "gu")
+    dc, ds, db = _weight(dn, "dn")
+    _cuda(expert_idx, (torch.int32,), "expert_idx")
+    _cuda(expert_w, (torch.float32,), "expert_w")
+    x = _cuda(x, _F16, "x")
+    _cuda(residual, _F16, "residual")
+    E, I2, H8 = gc.shape
+    I, H = I2 // 2, H8 * 8
+    if y is None:
+        y = torch.empty(H, dtype=torch.float16, device=x.device)
+    _cuda(err_flag, (torch.int32,), "err_flag")
+    st = lib.moe_qgemv_combine_noalloc(_ptr(gc), _ptr(gs), _ptr(gb), _ptr(dc), _ptr(ds),
+                                       _ptr(db), E, H, I, _ptr(expert_idx), _ptr(expert_w),
+                                       expert_idx.numel(), _ptr(x), _ptr(residual), _ptr(y),
+                                       _ptr(err_flag), _stream(stream))
+    _check(st, "moe_qgemv_combine_noalloc")
+    return y
+
+
+def noalloc_max_scratch_bytes() -> int:
+    return int(lib.qgemv_noalloc_max_scratch())
 
 
 def decode_attention_seq1(qkv, n_q, n_kv, head_dim, out=None, stream=None):

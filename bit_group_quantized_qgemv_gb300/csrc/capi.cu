@@ -259,6 +259,7 @@ const char* qgemv_strerror(int status) {
     case QGEMV_EALIGN: return "pointer misaligned (codes need 4 bytes, fp16 2 bytes)";
     case QGEMV_ELAUNCH: return "CUDA reported an error at kernel launch";
     case QGEMV_EDEVICE: return "no usable CUDA device";
+    case QGEMV_ESCRATCH: return "top_k * I exceeds the allocation-free scratch array";
     default: return "unknown status";
   }
 }

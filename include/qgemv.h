@@ -51,6 +51,7 @@ extern "C" {
 #define QGEMV_EALIGN (-3)  /* codes not 4-byte aligned, fp16 not 2-byte aligned */
 #define QGEMV_ELAUNCH (-4) /* CUDA reported an error at launch                */
 #define QGEMV_EDEVICE (-5) /* no usable CUDA device / device query failed     */
+#define QGEMV_ESCRATCH (-6) /* top_k * I exceeds the allocation-free scratch    */
 
 /* Largest supported small batch M and expert count top_k. */
 #define QGEMV_MAX_M 8
@@ -139,6 +140,44 @@ int moe_qgemv_combine(const uint32_t *gu_codes, const uint16_t *gu_scales,
 
 /* Workspace bytes moe_qgemv_combine needs: top_k * I fp32 values. */
 size_t qgemv_moe_workspace_bytes(int top_k, int I);
+
+/* Capacity of the allocation-free entry point's scratch, in fp32 values. */
+#define QGEMV_NOALLOC_MAX_SCRATCH 16384
+
+/*
+ * moe_qgemv_combine_noalloc -- moe_qgemv_combine without a workspace
+ * argument, for callers that cannot allocate device memory: for instance a
+ * plugin inside a host application that owns every device allocation and
+ * gives the plugin no allocator, or a latency-critical loop that must not
+ * allocate once it is running.  (The paper has no counterpart; this is an
+ * interface convenience of this library.)
+ *
+ * Instead of a caller workspace it uses one fixed scratch array of
+ * QGEMV_NOALLOC_MAX_SCRATCH fp32 values (64 KiB) in the library's own device
+ * memory.  Every GPU that loads the library holds that array until the
+ * process exits.  The call allocates nothing, and calls no cudaMalloc or
+ * cudaFree.
+ *   - top_k * I must be at most QGEMV_NOALLOC_MAX_SCRATCH, else
+ *     QGEMV_ESCRATCH; other arguments and checks as moe_qgemv_combine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: the first kernel writes every
+ *     value the second one reads.  Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on the array; serialise them.
+ * Results are identical to moe_qgemv_combine with a workspace.
+ */
+int moe_qgemv_combine_noalloc(const uint32_t *gu_codes, const uint16_t *gu_scales,
+                              const uint16_t *gu_biases, const uint32_t *dn_codes,
+                              const uint16_t *dn_scales, const uint16_t *dn_biases,
+                              int n_experts, int H, int I, const int32_t *expert_idx,
+                              const float *expert_w, int top_k, const uint16_t *x,
+                              const uint16_t *residual, uint16_t *y, int *err_flag,
+                              void *stream);
+
+/* Bytes of the allocation-free entry point's scratch array. */
+size_t qgemv_noalloc_max_scratch(void);
 
 /*
  * decode_attention_seq1 -- attention of one query over a single cached

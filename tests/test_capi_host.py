@@ -91,7 +91,7 @@ def test_misaligned_status(q):
 def test_workspace_bytes_and_strerror(q):
     assert q.moe_workspace_bytes(4, 1024) == 4 * 1024 * 4
     assert q.moe_workspace_bytes(0, 1024) == 0
-    for s in (0, -1, -2, -3, -4, -5):
+    for s in (0, -1, -2, -3, -4, -5, -6):
         assert q.strerror(s) and q.strerror(s) != "unknown status"
     assert q.strerror(-99) == "unknown status"
 
