@@ -7,7 +7,13 @@ ABI.  This package is the thin Python binding over that ABI.
 from ._binding import (  # noqa: F401
     EXPORTED,
     QgemvError,
+    StackLayer,
+    StackShape,
     decode_attention_seq1,
+    decode_stack,
+    decode_stack_workspace_bytes,
+    stack_layers,
+    stack_shape,
     device_status,
     last_cuda_error,
     lib,

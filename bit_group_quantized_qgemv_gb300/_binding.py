@@ -31,6 +31,8 @@ _SIGS = {
                                        _P, _P, _P]),
     "qgemv_noalloc_max_scratch": (ctypes.c_size_t, []),
     "decode_attention_seq1": (_I, [_P, _P, _I, _I, _I, _P]),
+    "qgemv_decode_stack_workspace_bytes": (ctypes.c_size_t, [_P]),
+    "qgemv_decode_stack": (_I, [_P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qgemv_strerror": (ctypes.c_char_p, [_I]),
     "qgemv_last_cuda_error": (_I, []),
     "qgemv_device_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
@@ -223,6 +225,63 @@ def decode_attention_seq1(qkv, n_q, n_kv, head_dim, out=None, stream=None):
                                    _stream(stream))
     _check(st, "decode_attention_seq1")
     return out
+
+
+_LAYER_FIELDS = ["qkv_codes", "qkv_scales", "qkv_biases", "attn_norm", "o_codes", "o_scales",
+                 "o_biases", "mlp_norm", "gate_codes", "gate_scales", "gate_biases", "up_codes",
+                 "up_scales", "up_biases", "down_codes", "down_scales", "down_biases"]
+
+
+class StackLayer(ctypes.Structure):
+    """qgemv_stack_layer: device pointers of one layer."""
+    _fields_ = [(f, ctypes.c_void_p) for f in _LAYER_FIELDS]
+
+
+class StackShape(ctypes.Structure):
+    """qgemv_stack_shape."""
+    _fields_ = [("hidden", _I), ("n_q", _I), ("n_kv", _I), ("head_dim", _I), ("inter", _I),
+                ("n_layers", _I), ("eps", _F)]
+
+
+def stack_shape(hidden, n_q, n_kv, head_dim, inter, n_layers, eps=1e-5) -> StackShape:
+    return StackShape(hidden, n_q, n_kv, head_dim, inter, n_layers, eps)
+
+
+def decode_stack_workspace_bytes(shape: StackShape) -> int:
+    return int(lib.qgemv_decode_stack_workspace_bytes(ctypes.byref(shape)))
+
+
+def stack_layers(layers):
+    """Descriptors for a list of layers, each a dict with weight triples
+    'qkv', 'o', 'gate', 'up', 'down' and fp16 vectors 'attn_norm',
+    'mlp_norm' (CUDA tensors)."""
+    arr = (StackLayer * len(layers))()
+    for i, L in enumerate(layers):
+        d = arr[i]
+        for name in ("qkv", "o", "gate", "up", "down"):
+            c, sc, b = _weight(L[name], name)
+            setattr(d, name + "_codes", c.data_ptr())
+            setattr(d, name + "_scales", sc.data_ptr())
+            setattr(d, name + "_biases", b.data_ptr())
+        d.attn_norm = _cuda(L["attn_norm"], _F16, "attn_norm").data_ptr()
+        d.mlp_norm = _cuda(L["mlp_norm"], _F16, "mlp_norm").data_ptr()
+    return arr
+
+
+def decode_stack(layers, shape: StackShape, x, y=None, workspace=None, stream=None):
+    """One token through the layer stack in one launch (qgemv_decode_stack).
+    `layers` is a list of layer dicts or a prebuilt stack_layers() array."""
+    arr = layers if isinstance(layers, ctypes.Array) else stack_layers(layers)
+    x = _cuda(x, _F16, "x")
+    if y is None:
+        y = torch.empty(shape.hidden, dtype=torch.float16, device=x.device)
+    nbytes = decode_stack_workspace_bytes(shape)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    st = lib.qgemv_decode_stack(arr, ctypes.byref(shape), _ptr(x), _ptr(y), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "qgemv_decode_stack")
+    return y
 
 
 def device_status() -> int:

@@ -272,7 +272,8 @@ int qgemv_device_status(unsigned* flags) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QGEMV_EDEVICE;
   unsigned v = 0;
   if (qgemv::status_plain(&v) != cudaSuccess || qgemv::status_norm_swiglu(&v) != cudaSuccess ||
-      qgemv::status_moe(&v) != cudaSuccess || qgemv::status_generic(&v) != cudaSuccess)
+      qgemv::status_moe(&v) != cudaSuccess || qgemv::status_generic(&v) != cudaSuccess ||
+      qgemv::status_stack(&v) != cudaSuccess)
     return QGEMV_EDEVICE;
   *flags = v;
   return QGEMV_OK;

@@ -140,5 +140,6 @@ cudaError_t status_plain(unsigned* out);
 cudaError_t status_norm_swiglu(unsigned* out);
 cudaError_t status_moe(unsigned* out);
 cudaError_t status_generic(unsigned* out);
+cudaError_t status_stack(unsigned* out);
 
 }  // namespace qgemv

@@ -1,0 +1,554 @@
+// stack.cu -- qgemv_decode_stack: one decode token through a whole stack of
+// pre-norm transformer layers' quantized matvecs in ONE persistent launch.
+//
+// Per layer l (INFERENCE_RESEARCH.md section 1: one command buffer encoding
+// the whole layer stack, fused kernels, no per-token overhead):
+//   op 0  qkv  = W_qkv . (x_l * gamma1) * rstd(x_l)          (RMSNorm fused)
+//   op 1  h    = x_l + W_o . attn,  attn = value heads of qkv (decode over
+//                one cached position: softmax of one score is 1)
+//   op 2  act  = silu(W_g . x~) * (W_u . x~),  x~ = h * gamma2 * rstd(h)
+//   op 3  x_{l+1} = h + W_d . act
+//
+// Why one launch: each op alone streams 9-66 MB and pays a fixed launch,
+// prologue and ring-fill cost of a few microseconds; 4 launches per layer
+// (5 with the value-head copy) x 32 layers made those fixed costs a large
+// part of the token.  Here the producer warp of every CTA streams the
+// weights of all ops of all layers back to back through one TMA ring
+// (weights never depend on activations), so the ring stays full across op
+// boundaries.  Only the consumers of an op wait, on a grid-wide counter, for
+// the op that produces their input; the epilogue warp publishes each op's
+// completion (fence + atomic).  The launch is cooperative, so every CTA is
+// resident and the counter waits can always complete; each wait is bounded
+// (~1 s) and sets the library status bit instead of hanging.
+#include <atomic>
+
+#include "qgemv.h"
+#include "qgemv_stream.cuh"
+
+namespace qgemv {
+namespace {
+
+constexpr int kMaxStackLayers = 64;
+constexpr int kStackJR = 4;
+constexpr int kOps = 4;  // qkv, o, gate.up, down
+
+struct StackLayerDev {
+  const uint8_t* w[5];  // qkv, o, gate, up, down codes
+  const __half* s[5];
+  const __half* b[5];
+  const __half* g1;  // attention norm
+  const __half* g2;  // MLP norm
+};
+
+struct OpPlanDev {
+  int K, rows, TG, S, RS, MS, stage_bytes, interleave;
+};
+
+struct StackArgs {
+  StackLayerDev layers[kMaxStackLayers];
+  OpPlanDev plan[kOps];
+  const __half* x_in;
+  __half* y_out;
+  __half* qkv;
+  __half* h;
+  __half* act;
+  __half* xbuf[2];
+  int* counters;  // [n_layers][4], zero on entry
+  int n_layers, H, n_q, n_kv, hd, I;
+  float eps;
+  int NS, slot_bytes, red_slot_floats;
+};
+
+// Ring position shared in lockstep by the three roles.
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  int ns;
+  __device__ explicit Ring(int ns_) : ns(ns_) {}
+  __device__ __forceinline__ void advance() {
+    if (++slot == ns) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// This CTA's rows of an op: contiguous range, or interleaved stages.
+struct OpRows {
+  int r0, r1, stride;
+};
+
+__device__ __forceinline__ OpRows op_rows(const OpPlanDev& p) {
+  OpRows o;
+  if (p.interleave) {
+    o.r0 = static_cast<int>(blockIdx.x) * p.RS;
+    o.r1 = p.rows;
+    o.stride = static_cast<int>(gridDim.x) * p.RS;
+  } else {
+    o.r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.rows / gridDim.x);
+    o.r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.rows / gridDim.x);
+    o.stride = 0;
+  }
+  return o;
+}
+
+__device__ __forceinline__ int next_row(const OpRows& o, int row, int n) {
+  return o.stride ? row + o.stride : row + n;
+}
+
+// Index of the op whose output op (l, k) reads, or -1 (the stack input).
+__device__ __forceinline__ int dependency(int l, int k) {
+  if (k == 0) return l == 0 ? -1 : (l - 1) * kOps + 3;
+  return l * kOps + k - 1;
+}
+
+// Bounded wait until *c >= target (gpu-scope acquire).
+__device__ bool wait_counter(const int* c, int target) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
+    if (global_timer_ns() - t0 > 1000000000ull) {
+      atomicOr(&g_status, kStatusWaitTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ const __half* op_input(const StackArgs& a, int l, int k) {
+  switch (k) {
+    case 0: return l == 0 ? a.x_in : a.xbuf[l & 1];
+    case 1: return a.qkv;
+    case 2: return a.h;
+    default: return a.act;
+  }
+}
+
+__device__ __forceinline__ const __half* layer_input(const StackArgs& a, int l) {
+  return l == 0 ? a.x_in : a.xbuf[l & 1];
+}
+
+template <int JR>
+__global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ StackArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t part_bar[kMaxStages];
+  __shared__ int s_abort;
+
+  const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NS = a.NS;
+  const int P = static_cast<int>(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&part_bar[s]), static_cast<uint32_t>(T / 32));
+      mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32 + 1));
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(NS) * a.slot_bytes);
+  __half* x_sm = reinterpret_cast<__half*>(red + static_cast<size_t>(NS) * a.red_slot_floats);
+
+  // ------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      Ring ring(NS);
+      int issued = 0;
+      bool ok = true;
+      for (int l = 0; l < a.n_layers && ok; ++l) {
+        const StackLayerDev& L = a.layers[l];
+        for (int k = 0; k < kOps && ok; ++k) {
+          const OpPlanDev& p = a.plan[k];
+          const int rcb = p.K / 2, rgb = p.K / 32;
+          const int scales_off = p.MS * p.RS * rcb;
+          const int biases_off = scales_off + p.MS * p.RS * rgb;
+          const OpRows o = op_rows(p);
+          for (int row = o.r0; row < o.r1;) {
+            const int n = min(p.RS, o.r1 - row);
+            if (!mbar_wait(smem_u32(&empty_bar[ring.slot]), ring.phase ^ 1u, &g_status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full_bar[ring.slot]);
+            const uint32_t st = smem_u32(smem + static_cast<size_t>(ring.slot) * a.slot_bytes);
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.MS * n * (rcb + 2 * rgb)));
+            for (int m = 0; m < p.MS; ++m) {
+              const int wi = (k == 0) ? 0 : (k == 1) ? 1 : (k == 2) ? 2 + m : 4;
+              bulk_g2s(st + m * p.RS * rcb, L.w[wi] + static_cast<long long>(row) * rcb, n * rcb,
+                       fb, pol);
+              bulk_g2s(st + scales_off + m * p.RS * rgb, L.s[wi] + static_cast<long long>(row) * (rgb / 2),
+                       n * rgb, fb, pol);
+              bulk_g2s(st + biases_off + m * p.RS * rgb, L.b[wi] + static_cast<long long>(row) * (rgb / 2),
+                       n * rgb, fb, pol);
+            }
+            ++issued;
+            ring.advance();
+            row = next_row(o, row, n);
+          }
+        }
+      }
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        mbar_wait(smem_u32(&full_bar[j % NS]), (j / NS) & 1, &g_status);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ epilogue
+  if (warp == 1) {
+    Ring ring(NS);
+    for (int l = 0; l < a.n_layers; ++l) {
+      for (int k = 0; k < kOps; ++k) {
+        const OpPlanDev& p = a.plan[k];
+        const int dep = dependency(l, k);
+        // Every lane acquires the producing op's completion itself.
+        const int ok = (dep >= 0) ? wait_counter(a.counters + dep, P) : 1;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        // RMS of the op's normalised input (ops 0 and 2).
+        float rstd = 1.f;
+        if (k == 0 || k == 2) {
+          const __half* xin = (k == 0) ? layer_input(a, l) : a.h;
+          float sq = 0.f;
+          for (int i = lane; i < a.H; i += 32) {
+            const float v = __half2float(xin[i]);
+            sq = fmaf(v, v, sq);
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+          rstd = 1.0f / sqrtf(sq / static_cast<float>(a.H) + a.eps);
+        }
+        const int wpt = p.TG >> 5;
+        const OpRows o = op_rows(p);
+        __half* out = (k == 0) ? a.qkv
+                      : (k == 1) ? a.h
+                      : (k == 2) ? a.act
+                                 : (l == a.n_layers - 1 ? a.y_out : a.xbuf[(l + 1) & 1]);
+        const __half* resid = (k == 1) ? layer_input(a, l) : (k == 3) ? a.h : nullptr;
+        for (int row = o.r0; row < o.r1;) {
+          const int n = min(p.RS, o.r1 - row);
+          if (!mbar_wait(smem_u32(&part_bar[ring.slot]), ring.phase, &g_status)) return;
+          const float* rs = red + static_cast<size_t>(ring.slot) * a.red_slot_floats;
+          for (int r = lane; r < n; r += 32) {
+            float v0 = 0.f, v1 = 0.f;
+            for (int w = 0; w < wpt; ++w) v0 += rs[r * wpt + w];
+            if (p.MS == 2)
+              for (int w = 0; w < wpt; ++w) v1 += rs[(p.RS + r) * wpt + w];
+            v0 *= kTwo24;
+            v1 *= kTwo24;
+            const int gr = row + r;
+            float res;
+            if (k == 0) {
+              res = v0 * rstd;
+            } else if (k == 2) {
+              res = silu_f(v0 * rstd) * (v1 * rstd);
+            } else {
+              res = v0 + __half2float(resid[gr]);
+            }
+            out[gr] = __float2half_rn(res);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[ring.slot]));
+          ring.advance();
+          row = next_row(o, row, n);
+        }
+        // This CTA's rows of op (l, k) are written: publish.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.counters + l * kOps + k, 1);
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- consumers
+  const int t = threadIdx.x - 64;
+  Ring ring(NS);
+  for (int l = 0; l < a.n_layers; ++l) {
+    const StackLayerDev& L = a.layers[l];
+    for (int k = 0; k < kOps; ++k) {
+      const OpPlanDev& p = a.plan[k];
+      const int dep = dependency(l, k);
+      // Input ready everywhere, and every consumer done with the previous op.
+      if (dep >= 0 && t == 0) {
+        if (!wait_counter(a.counters + dep, P)) s_abort = 1;
+        __threadfence();
+      }
+      named_bar_sync(2, T);
+      if (*reinterpret_cast<volatile int*>(&s_abort) != 0) return;
+
+      // Convert the op's input into shared memory (fp16 in k order) and
+      // sum each 32-k slice.  ops 0 and 2 multiply by gamma here; rstd is
+      // applied by the epilogue warp.  op 1 gathers the value heads.
+      const int K = p.K;
+      const __half* gam = (k == 0) ? L.g1 : (k == 2) ? L.g2 : nullptr;
+      float* xsum_sm = reinterpret_cast<float*>(x_sm + K);
+      for (int gi = t; gi < K / 8; gi += T) {  // lane-uniform trip count
+        const int k0 = gi * 8;
+        const __half* src;
+        if (k == 1) {
+          const int head = k0 / a.hd;
+          src = a.qkv + static_cast<long long>(a.n_q + a.n_kv + head / (a.n_q / a.n_kv)) * a.hd +
+                (k0 - head * a.hd);
+        } else {
+          src = op_input(a, l, k) + k0;
+        }
+        const uint4 raw = *reinterpret_cast<const uint4*>(src);
+        const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+        float xv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(hv[j]);
+          xv[2 * j] = f.x;
+          xv[2 * j + 1] = f.y;
+        }
+        if (gam != nullptr) {
+          const uint4 graw = *reinterpret_cast<const uint4*>(gam + k0);
+          const __half2* gv = reinterpret_cast<const __half2*>(&graw);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(gv[j]);
+            xv[2 * j] *= f.x;
+            xv[2 * j + 1] *= f.y;
+          }
+        }
+        uint4 packed;
+        uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half lo = __float2half_rn(xv[2 * j]), hi = __float2half_rn(xv[2 * j + 1]);
+          pw[j] = pack_half2(lo, hi);
+          part += __half2float(lo) + __half2float(hi);
+        }
+        *reinterpret_cast<uint4*>(x_sm + k0) = packed;
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if ((lane & 3) == 0) xsum_sm[gi / 4] = part;
+      }
+      named_bar_sync(2, T);
+
+      // This op's thread mapping.
+      const int TG = p.TG, S = p.S;
+      const bool active = t < S * TG;  // whole warps
+      const int slot = active ? t / TG : 0;
+      const int uu = active ? t - slot * TG : 0;
+      const int wit = uu >> 5, wpt = TG >> 5;
+      const int rcb = K / 2, rgb = K / 32;
+      const int scales_off = p.MS * p.RS * rcb;
+      const int biases_off = scales_off + p.MS * p.RS * rgb;
+      unsigned short xr[kSliceK];
+      float xs_scaled = 0.f;
+      int task_row[JR], code_off[JR], group_off[JR];
+      if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(x_sm + uu * kSliceK);
+#pragma unroll
+        for (int i = 0; i < kSliceK / 8; ++i) {
+          const uint4 v = src[i];
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            xr[8 * i + 2 * j] = static_cast<unsigned short>(w4[j] & 0xffffu);
+            xr[8 * i + 2 * j + 1] = static_cast<unsigned short>(w4[j] >> 16);
+          }
+        }
+        xs_scaled = xsum_sm[uu] * kTwoM24;
+      }
+      const int group_in_row = (uu * kSliceK) / 64;
+#pragma unroll
+      for (int j = 0; j < JR; ++j) {
+        const int task = slot + j * S;
+        const int ms = task / p.RS;
+        const int rl = task - ms * p.RS;
+        task_row[j] = rl;
+        code_off[j] = (ms * p.RS + rl) * rcb + uu * 16;
+        group_off[j] = (ms * p.RS + rl) * rgb + group_in_row * 2;
+      }
+
+      const OpRows o = op_rows(p);
+      for (int row = o.r0; row < o.r1;) {
+        const int n = min(p.RS, o.r1 - row);
+        if (!mbar_wait(smem_u32(&full_bar[ring.slot]), ring.phase, &g_status)) return;
+        if (active) {
+          const uint8_t* st = smem + static_cast<size_t>(ring.slot) * a.slot_bytes;
+          float acc[JR];
+#pragma unroll
+          for (int j = 0; j < JR; ++j) {
+            const __half sv = *reinterpret_cast<const __half*>(st + scales_off + group_off[j]);
+            const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
+            const float v = slice_dot<4>(st + code_off[j], xr, __half2float(sv), __half2float(bv),
+                                         xs_scaled);
+            acc[j] = task_row[j] < n ? v : 0.f;
+          }
+          float* rs = red + static_cast<size_t>(ring.slot) * a.red_slot_floats;
+          constexpr int kLanesPerRow = 32 / JR;
+          const float v = warp_reduce_rows<JR>(acc, lane);
+          if ((lane & (kLanesPerRow - 1)) == 0)
+            rs[(slot + (lane / kLanesPerRow) * S) * wpt + wit] = v;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&part_bar[ring.slot]));
+          mbar_arrive(smem_u32(&empty_bar[ring.slot]));
+        }
+        ring.advance();
+        row = next_row(o, row, n);
+      }
+    }
+  }
+}
+
+std::atomic<unsigned> g_attr_done{0};
+
+}  // namespace
+}  // namespace qgemv
+
+extern "C" {
+
+size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape* shape) {
+  if (shape == nullptr || shape->n_layers < 1) return 0;
+  auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  const size_t nqkv = static_cast<size_t>(shape->n_q + 2 * shape->n_kv) * shape->head_dim;
+  return up(sizeof(int) * 4 * static_cast<size_t>(shape->n_layers)) + up(2 * nqkv) +
+         up(2 * static_cast<size_t>(shape->hidden)) + up(2 * static_cast<size_t>(shape->inter)) +
+         2 * up(2 * static_cast<size_t>(shape->hidden));
+}
+
+int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape* shape,
+                       const uint16_t* x, uint16_t* y, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  using namespace qgemv;
+  if (!layers || !shape || !x || !y || !workspace) return QGEMV_ENULL;
+  const int H = shape->hidden, nq = shape->n_q, nkv = shape->n_kv, hd = shape->head_dim;
+  const int I = shape->inter, NL = shape->n_layers;
+  if (NL < 1 || NL > kMaxStackLayers || nq < 1 || nkv < 1 || nq % nkv != 0 || hd < 8 ||
+      hd % 8 != 0 || !(shape->eps > 0.0f))
+    return QGEMV_EINVAL;
+  const int Dq = nq * hd;
+  const int nqkv = (nq + 2 * nkv) * hd;
+  for (int K : {H, Dq, I})
+    if (K % 1024 != 0 || K / kSliceK > 512) return QGEMV_EINVAL;
+  if (workspace_bytes < qgemv_decode_stack_workspace_bytes(shape)) return QGEMV_EINVAL;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!al16(x) || !al16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return QGEMV_EALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return QGEMV_EDEVICE;
+
+  StackArgs a{};
+  for (int l = 0; l < NL; ++l) {
+    const qgemv_stack_layer& s = layers[l];
+    const uint32_t* w[5] = {s.qkv_codes, s.o_codes, s.gate_codes, s.up_codes, s.down_codes};
+    const uint16_t* sc[5] = {s.qkv_scales, s.o_scales, s.gate_scales, s.up_scales, s.down_scales};
+    const uint16_t* bi[5] = {s.qkv_biases, s.o_biases, s.gate_biases, s.up_biases, s.down_biases};
+    for (int m = 0; m < 5; ++m) {
+      if (!w[m] || !sc[m] || !bi[m]) return QGEMV_ENULL;
+      if (!al16(w[m]) || !al16(sc[m]) || !al16(bi[m])) return QGEMV_EALIGN;
+      a.layers[l].w[m] = reinterpret_cast<const uint8_t*>(w[m]);
+      a.layers[l].s[m] = reinterpret_cast<const __half*>(sc[m]);
+      a.layers[l].b[m] = reinterpret_cast<const __half*>(bi[m]);
+    }
+    if (!s.attn_norm || !s.mlp_norm) return QGEMV_ENULL;
+    if (!al16(s.attn_norm) || !al16(s.mlp_norm)) return QGEMV_EALIGN;
+    a.layers[l].g1 = reinterpret_cast<const __half*>(s.attn_norm);
+    a.layers[l].g2 = reinterpret_cast<const __half*>(s.mlp_norm);
+  }
+  // Plans of the four ops (same for every layer), all with JR = 4.
+  const int kinds[kOps] = {kNorm, kPlain, kSwiglu, kPlain};
+  const int Ks[kOps] = {H, Dq, H, I};
+  const int rows[kOps] = {nqkv, H, I, H};
+  int slot_bytes = 0, red_floats = 0, x_bytes = 0;
+  for (int k = 0; k < kOps; ++k) {
+    const StreamPlan p = make_stream_plan(kinds[k], 4, Ks[k], rows[k], 1, sms, 512, kStackJR);
+    if (!p.ok || p.jr != kStackJR) return QGEMV_EINVAL;
+    OpPlanDev& d = a.plan[k];
+    d.K = Ks[k];
+    d.rows = rows[k];
+    d.TG = p.tg;
+    d.S = p.s;
+    d.RS = p.rs;
+    d.MS = (k == 2) ? 2 : 1;
+    d.stage_bytes = p.stage_bytes;
+    d.interleave = p.interleave;
+    slot_bytes = slot_bytes > p.stage_bytes ? slot_bytes : p.stage_bytes;
+    const int rf = ((p.s * p.jr * (p.tg / 32)) + 3) & ~3;
+    red_floats = red_floats > rf ? red_floats : rf;
+    const int xb = Ks[k] * 2 + (Ks[k] / kSliceK) * 4;
+    x_bytes = x_bytes > xb ? x_bytes : xb;
+  }
+  int ns = (200 * 1024 - x_bytes) / (slot_bytes + red_floats * 4);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) return QGEMV_EINVAL;
+  a.NS = ns;
+  a.slot_bytes = slot_bytes;
+  a.red_slot_floats = red_floats;
+  const int smem = ns * (slot_bytes + red_floats * 4) + x_bytes;
+
+  // Workspace: counters, qkv, h, act, x ping-pong.
+  auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  uint8_t* wp = static_cast<uint8_t*>(workspace);
+  a.counters = reinterpret_cast<int*>(wp);
+  wp += up(sizeof(int) * 4 * static_cast<size_t>(NL));
+  a.qkv = reinterpret_cast<__half*>(wp);
+  wp += up(2 * static_cast<size_t>(nqkv));
+  a.h = reinterpret_cast<__half*>(wp);
+  wp += up(2 * static_cast<size_t>(H));
+  a.act = reinterpret_cast<__half*>(wp);
+  wp += up(2 * static_cast<size_t>(I));
+  a.xbuf[0] = reinterpret_cast<__half*>(wp);
+  wp += up(2 * static_cast<size_t>(H));
+  a.xbuf[1] = reinterpret_cast<__half*>(wp);
+  a.x_in = reinterpret_cast<const __half*>(x);
+  a.y_out = reinterpret_cast<__half*>(y);
+  a.n_layers = NL;
+  a.H = H;
+  a.n_q = nq;
+  a.n_kv = nkv;
+  a.hd = hd;
+  a.I = I;
+  a.eps = shape->eps;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* kern = stack_kernel<kStackJR>;
+  if (dev < 32 && !((g_attr_done.load(std::memory_order_acquire) >> dev) & 1u)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024) !=
+        cudaSuccess)
+      return QGEMV_ELAUNCH;
+    g_attr_done.fetch_or(1u << dev, std::memory_order_acq_rel);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 576, smem) != cudaSuccess ||
+      per_sm < 1)
+    return QGEMV_ELAUNCH;
+  if (cudaMemsetAsync(a.counters, 0, sizeof(int) * 4 * static_cast<size_t>(NL), st) != cudaSuccess)
+    return QGEMV_ELAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  cfg.blockDim = dim3(576);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return QGEMV_ELAUNCH;
+  return QGEMV_OK;
+}
+
+}  // extern "C"
+
+namespace qgemv {
+cudaError_t status_stack(unsigned* out) { return read_clear_status(out); }
+}  // namespace qgemv

@@ -192,6 +192,58 @@ size_t qgemv_noalloc_max_scratch(void);
 int decode_attention_seq1(const uint16_t *qkv, uint16_t *out, int n_q, int n_kv,
                           int head_dim, void *stream);
 
+/*
+ * Decode stack: one token through a stack of pre-norm transformer layers'
+ * quantized matvecs in one launch.  INFERENCE_RESEARCH.md section 1: encode
+ * the whole layer stack at once, fused kernels, zero per-token overhead.
+ * Per layer l, with 4-bit g64 weights and fp16 activations:
+ *   qkv     = W_qkv . rmsnorm(x_l; attn_norm)              [(n_q+2 n_kv) hd]
+ *   attn    = value heads of qkv, head h -> value head h/(n_q/n_kv)
+ *             (decode over one cached position: softmax of one score is 1)
+ *   h       = x_l + W_o . attn                              [hidden]
+ *   act     = silu(W_gate . r) * (W_up . r), r = rmsnorm(h; mlp_norm)  [inter]
+ *   x_{l+1} = h + W_down . act                              [hidden]
+ * with rmsnorm(v; g) = v * g / sqrt(mean(v^2) + eps).  Same arithmetic and
+ * roundings as rmsnorm_qgemv, decode_attention_seq1, qgemv_w4g64 and
+ * swiglu_qgemv chained.
+ */
+typedef struct {
+  const uint32_t *qkv_codes;   /* [(n_q + 2 n_kv) * head_dim][hidden/8]  */
+  const uint16_t *qkv_scales, *qkv_biases;
+  const uint16_t *attn_norm;   /* [hidden] fp16 */
+  const uint32_t *o_codes;     /* [hidden][n_q * head_dim / 8]           */
+  const uint16_t *o_scales, *o_biases;
+  const uint16_t *mlp_norm;    /* [hidden] fp16 */
+  const uint32_t *gate_codes;  /* [inter][hidden/8]                      */
+  const uint16_t *gate_scales, *gate_biases;
+  const uint32_t *up_codes;    /* [inter][hidden/8]                      */
+  const uint16_t *up_scales, *up_biases;
+  const uint32_t *down_codes;  /* [hidden][inter/8]                      */
+  const uint16_t *down_scales, *down_biases;
+} qgemv_stack_layer;
+
+typedef struct {
+  int hidden, n_q, n_kv, head_dim, inter, n_layers;
+  float eps;
+} qgemv_stack_shape;
+
+/* Workspace bytes qgemv_decode_stack needs (counters, qkv, h, act, x). */
+size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape *shape);
+
+/*
+ * qgemv_decode_stack -- y = stack(x).  `layers` is a HOST array of n_layers
+ * descriptors of device pointers (all 16-byte aligned); x, y [hidden] fp16
+ * device (16-byte aligned, may not overlap the workspace); workspace:
+ * device, 256-byte aligned, >= qgemv_decode_stack_workspace_bytes bytes,
+ * contents on entry ignored.  Checks: 1 <= n_layers <= 64, n_q % n_kv == 0,
+ * head_dim % 8 == 0, hidden, n_q*head_dim and inter multiples of 1024 and at
+ * most 16384, eps > 0.  Enqueues a memset of the workspace's counters and
+ * one cooperative launch on `stream`.
+ */
+int qgemv_decode_stack(const qgemv_stack_layer *layers, const qgemv_stack_shape *shape,
+                       const uint16_t *x, uint16_t *y, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
 /* Human-readable text for a status code (static string). */
 const char *qgemv_strerror(int status);
 
