@@ -3,24 +3,25 @@
 
 Workload: one decode token (batch 1) through a stack of 32
 Llama-3.1-8B-shaped layers, each the fused matvec chain
-    rmsnorm_qgemv(QKV 4096->6144) -> decode_attention_seq1 (value-head copy)
-    -> qgemv_w4g64(o_proj 4096->4096, + residual)
-    -> swiglu_qgemv(gate.up 4096->2x14336, post-attention RMSNorm fused)
-    -> qgemv_w4g64(down 14336->4096, + residual)
+    RMSNorm->QKV 4096->6144 -> value-head copy (decode over one position)
+    -> o_proj 4096->4096 (+ residual)
+    -> gate.up 4096->2x14336 SwiGLU (post-attention RMSNorm fused)
+    -> down 14336->4096 (+ residual)
 with 4-bit group-64 planar weights.  A step is one token through all 32
-layers (3.93 GB of distinct device weights, so no step's inputs fit in the
-129 MB L2).  The 32 layers are device copies of one seeded synthetic layer.
+layers: ONE qgemv_decode_stack launch (persistent, cooperative) reading
+3.93 GB of distinct device weights, so no step's inputs fit in the 129 MB
+L2.  The 32 layers are device copies of one seeded synthetic layer.
 
 Metric: algorithmic HBM GB/s (codes + scales + biases + activations read and
 written, per the byte accounting of bit_group_quantized_qgemv_gb300.accounting)
 divided by the device time of the step, plus us per decode matvec stack.
 
-Timing: the step is captured once as a CUDA graph of C-ABI calls; W warm-up
-and K timed replays on one stream, CUDA events around the K, a barrier and
-torch.cuda.synchronize() on both sides, max over ranks.  Events captured
-around every gate.up SwiGLU launch give the dominant kernel's live duration.
-`--impl reference` times the fp64 CPU oracle on a bounded row sample of the
-same layer instead.
+Timing: W warm-up and K timed steps on one stream, CUDA events around the K,
+a barrier and torch.cuda.synchronize() on both sides, max over ranks.  The
+same chain as a CUDA graph of single-op C-ABI launches (5 per layer) is
+timed beside it ("unfused").  `--op NAME` times one fused op alone through
+CUDA-graph replays.  `--impl reference` times the fp64 CPU oracle on a
+bounded row sample of the same layer instead.
 """
 from __future__ import annotations
 
@@ -51,6 +52,10 @@ def parse_args():
     p.add_argument("--layers", type=int, default=LAYERS)
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip the oracle CPU-baseline leg")
+    p.add_argument("--no-unfused", action="store_true",
+                   help="skip the single-op CUDA-graph comparison")
+    p.add_argument("--op", choices=["stack", "qkv", "o_proj", "swiglu", "down", "moe"],
+                   default="stack", help="time one fused op alone instead of the stack")
     return p.parse_args()
 
 
@@ -142,7 +147,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ own arm
-def build_stack(q, torch, n_layers, device):
+def build_stack(torch, n_layers, device):
     import numpy as np
 
     import synth
@@ -160,7 +165,7 @@ def build_stack(q, torch, n_layers, device):
     layers = []
     for _ in range(n_layers):
         layers.append({k: tuple(t.clone() for t in v) for k, v in base.items()} |
-                      {"gamma1": g1.clone(), "gamma2": g2.clone()})
+                      {"attn_norm": g1.clone(), "mlp_norm": g2.clone()})
     x0 = torch.from_numpy(layer["x"]).to(device)
     bufs = {
         "x": torch.empty(H, dtype=torch.float16, device=device),
@@ -173,20 +178,17 @@ def build_stack(q, torch, n_layers, device):
     return layers, x0, bufs
 
 
-def step_calls(q, layers, bufs, eps, events=None):
-    """Enqueue one token through the stack (C-ABI calls on the current stream)."""
+def unfused_calls(q, layers, bufs, eps):
+    """The same token as single-op C-ABI calls (5 per layer) on the current
+    stream, for the comparison graph."""
     import synth
     c = synth.LLAMA8B
     x, qkv, attn, h, act = bufs["x"], bufs["qkv"], bufs["attn"], bufs["h"], bufs["act"]
-    for li, L in enumerate(layers):
-        q.rmsnorm_qgemv(L["qkv"], x, L["gamma1"], eps, y=qkv)
+    for L in layers:
+        q.rmsnorm_qgemv(L["qkv"], x, L["attn_norm"], eps, y=qkv)
         q.decode_attention_seq1(qkv, c["n_q"], c["n_kv"], c["head_dim"], out=attn)
         q.qgemv_w4g64(L["o"], attn, y=h, residual=x)
-        if events is not None:
-            events[li][0].record()
-        q.swiglu_qgemv(L["gate"], L["up"], h, L["gamma2"], eps, h=act)
-        if events is not None:
-            events[li][1].record()
+        q.swiglu_qgemv(L["gate"], L["up"], h, L["mlp_norm"], eps, h=act)
         q.qgemv_w4g64(L["down"], act, y=x, residual=h)
 
 
@@ -197,6 +199,7 @@ def run_own(args):
     __graft_entry__.build()
     import bit_group_quantized_qgemv_gb300 as q
     from bit_group_quantized_qgemv_gb300 import accounting as acc
+    import synth
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -210,89 +213,102 @@ def run_own(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    c = synth.LLAMA8B
     n_layers = args.layers
     eps = 1e-5
-    layers, x0, bufs = build_stack(q, torch, n_layers, device)
+    layers, x0, bufs = build_stack(torch, n_layers, device)
     ops = acc.llama8b_layer_ops(4)
-    layer_bytes = sum(b for _, b in ops) + 2 * 2 * 128 * 32  # + the value-head copy
+    layer_bytes = acc.llama8b_layer_bytes(4)
     step_bytes = n_layers * layer_bytes
-    swiglu_bytes = dict(ops)["gate_up_swiglu"]
+    shape = q.stack_shape(c["hidden"], c["n_q"], c["n_kv"], c["head_dim"], c["inter"], n_layers,
+                          eps)
+    descs = q.stack_layers(layers)
+    work = torch.empty(q.decode_stack_workspace_bytes(shape), dtype=torch.uint8, device=device)
+    x_in = x0.clone()
+    y_out = torch.empty_like(x0)
 
     stream = torch.cuda.Stream(device)
+
+    def step():
+        q.decode_stack(descs, shape, x_in, y=y_out, workspace=work, stream=stream)
+
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        bufs["x"].copy_(x0)
-        step_calls(q, layers, bufs, eps)          # eager warm-up (sets kernel attributes)
+    step()                                        # sets the kernel's attributes
     torch.cuda.synchronize()
     if q.device_status() != 0:
         raise RuntimeError("device-side wait timed out during warm-up")
 
-    def timing_event():
-        # external=True makes a record inside graph capture a real event node
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return torch.cuda.Event(enable_timing=True)
-
-    # One graph per ring slot, each with its own events around gate.up SwiGLU.
-    ring = 4
-    graphs, evsets = [], []
-    for _ in range(ring):
-        ev = [(timing_event(), timing_event()) for _ in range(n_layers)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step_calls(q, layers, bufs, eps, ev)
-        graphs.append(g)
-        evsets.append(ev)
-    # End-to-end graph: H2D of the token's input from pinned host memory,
-    # the stack, D2H of its output.
-    x_host = x0.cpu().pin_memory()
-    y_host = torch.empty_like(x_host).pin_memory()
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        bufs["x"].copy_(x_host, non_blocking=True)
-        step_calls(q, layers, bufs, eps)
-        y_host.copy_(bufs["x"], non_blocking=True)
-    torch.cuda.synchronize()
-
     K, W = args.steps, args.warmup
-    gpu_id = "0"
+    gpu_id = str(local)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
-        gpu_id = str(local)
+        pass
 
-    # ---- timed region: K steps of the device-resident stack
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            graphs[i % ring].replay()
+    # ---- timed region: K steps of the device-resident stack, one launch each
+    for _ in range(W):
+        step()
     barrier()
     clocks = ClockSampler(gpu_id)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t_start.record()
-        for i in range(K):
-            graphs[i % ring].replay()
-        t_end.record()
+    t_start.record(stream)
+    for _ in range(K):
+        step()
+    t_end.record(stream)
     barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
-    swiglu_ms = [a.elapsed_time(b) for ev in evsets for a, b in ev]
-    # ---- timed region: end to end with host buffers
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    # ---- timed region: end to end through the public API with host buffers
+    x_host = x0.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+
+    def step_e2e():
+        with torch.cuda.stream(stream):
+            x_in.copy_(x_host, non_blocking=True)
+            step()
+            y_host.copy_(y_out, non_blocking=True)
+
     Ke = max(1, min(K, 1000))
-    with torch.cuda.stream(stream):
-        for _ in range(min(W, 20)):
-            g_e2e.replay()
+    for _ in range(min(W, 20)):
+        step_e2e()
     barrier()
-    with torch.cuda.stream(stream):
-        e0.record()
-        for _ in range(Ke):
-            g_e2e.replay()
-        e1.record()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        step_e2e()
+    e1.record(stream)
     barrier()
     ms_e2e = e0.elapsed_time(e1)
     out_ok = bool(torch.isfinite(y_host.float()).all())
+
+    # ---- the same token as a CUDA graph of single-op launches
+    unfused = None
+    if not args.no_unfused:
+        with torch.cuda.stream(stream):
+            bufs["x"].copy_(x0)
+            unfused_calls(q, layers, bufs, eps)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            unfused_calls(q, layers, bufs, eps)
+        Ku = max(1, min(K, 1000))
+        with torch.cuda.stream(stream):
+            for _ in range(min(W, 20)):
+                g.replay()
+        barrier()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(Ku):
+                g.replay()
+        u1.record(stream)
+        barrier()
+        ms_u = u0.elapsed_time(u1) / Ku
+        unfused = {"us_per_step": round(ms_u * 1e3, 2),
+                   "value": round(step_bytes / (ms_u * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "launches_per_step": 5 * n_layers,
+                   "how": "CUDA graph of 5 single-op C-ABI launches per layer"}
     status = q.device_status()
 
     if world > 1:
@@ -303,8 +319,8 @@ def run_own(args):
     peak, peak_kind = measured_peak()
     value = world * step_bytes * K / (ms * 1e-3) / 1e9
     e2e_value = world * step_bytes * Ke / (ms_e2e * 1e-3) / 1e9
-    sw_ms = statistics.mean(swiglu_ms)
-    achieved = swiglu_bytes / (sw_ms * 1e-3) / 1e9
+    launch_ms = ms / K
+    achieved = step_bytes / (launch_ms * 1e-3) / 1e9
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -320,13 +336,14 @@ def run_own(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "fp16 activations, 4-bit g64 weights, fp32 accumulate",
-        "data": "synthetic (seeded; 32 device copies of one Llama-3.1-8B-shaped layer)",
+        "data": "synthetic (seeded; %d device copies of one Llama-3.1-8B-shaped layer)" % n_layers,
         "config": {
             "workload": "Llama-3.1-8B-shaped decode layer x%d, w4g64, batch 1" % n_layers,
             "layers_per_step": n_layers,
             "bytes_per_step": step_bytes,
             "l2": "inputs larger than L2: %.2f GB of distinct weights per step" % (step_bytes / 1e9),
-            "timing": "CUDA graph of C-ABI calls per step, CUDA events on the launching stream",
+            "timing": "one qgemv_decode_stack launch per step (persistent, cooperative); "
+                      "CUDA events on the launching stream",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "us_per_step": round(ms / K * 1e3, 2),
@@ -336,17 +353,18 @@ def run_own(args):
         "peak_kind": peak_kind,
         "tok_s": round(1e3 * K / ms, 1),
         "roofline": {
-            "kernel": "swiglu_qgemv (gate.up 4096 -> 2 x 14336, RMSNorm fused)",
+            "kernel": "qgemv_decode_stack (stack_kernel, one launch per token, %d layers)" % n_layers,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic("swiglu_qgemv_llama8b"),
-            "algorithmic_bytes_per_launch": swiglu_bytes,
-            "avg_launch_us": round(sw_ms * 1e3, 3),
-            "launches_timed": len(swiglu_ms),
-            "peak_note": "of %s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
+            "traffic": recorded_traffic("decode_stack_llama8b"),
+            "algorithmic_bytes_per_launch": step_bytes,
+            "avg_launch_us": round(launch_ms * 1e3, 3),
+            "launches_timed": K,
+            "peak_note": "of %s (MEASURED_PEAKS.json hbm_gbs); launch time includes the "
+                         "counter memset enqueued with it" % peak_kind,
         },
         "cpu_baseline": cpu,
         "e2e": {
@@ -355,9 +373,10 @@ def run_own(args):
             "h2d_bytes_per_step": int(x_host.numel() * 2),
             "d2h_bytes_per_step": int(y_host.numel() * 2),
             "steps": Ke,
-            "how": "CUDA graph per token: pinned-host H2D of x, the stack via C-ABI calls, D2H of y",
+            "how": "per token: pinned-host H2D of x, qgemv_decode_stack, D2H of y",
         },
-        "gpu_launches": K * n_layers * 5,
+        "unfused": unfused,
+        "gpu_launches": K,
         "clocks": clk,
         "device_status": status,
         "output_finite": out_ok,
@@ -366,6 +385,97 @@ def run_own(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_op(args):
+    """One fused op of the Llama-8B-shaped layer (or one MoE token), timed
+    alone: a CUDA graph of launches on rotating device copies (more bytes
+    than L2), replayed; one JSON line."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_group_quantized_qgemv_gb300 as q
+    from bit_group_quantized_qgemv_gb300 import accounting as acc
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    eps = 1e-5
+
+    def up(w):
+        return (torch.from_numpy(np.ascontiguousarray(w.codes).view(np.int32)).to(dev),
+                torch.from_numpy(w.scales).to(dev), torch.from_numpy(w.biases).to(dev))
+
+    layer = synth.llama_layer(1, 0, 4)
+    H, I = synth.LLAMA8B["hidden"], synth.LLAMA8B["inter"]
+    x = torch.from_numpy(layer["x"]).to(dev)
+    g1 = torch.from_numpy(layer["gamma1"]).to(dev)
+    g2 = torch.from_numpy(layer["gamma2"]).to(dev)
+    ops = dict(acc.llama8b_layer_ops(4))
+    if args.op == "moe":
+        gu, dn = synth.moe_experts(3, 0, 8)
+        base = (up(gu), up(dn))
+        nbytes = acc.moe_token_bytes()
+    elif args.op == "swiglu":
+        base = (up(layer["gate"]), up(layer["up"]))
+        nbytes = ops["gate_up_swiglu"]
+    else:
+        key = {"qkv": "qkv", "o_proj": "o", "down": "down"}[args.op]
+        base = (up(layer[key]),)
+        nbytes = ops[{"qkv": "rmsnorm_qkv", "o_proj": "o_proj_residual",
+                      "down": "down_residual"}[args.op]]
+    copies = max(2, int(3 * 129e6 // nbytes) + 1)
+    ws = [tuple(tuple(t.clone() for t in w) for w in base) for _ in range(copies)]
+    xi = torch.randn(I, device=dev).half()
+    y = torch.empty(max(I, 6144), device=dev).half()
+    idx = torch.tensor([0, 3, 5, 6], dtype=torch.int32, device=dev)
+    wt = torch.tensor([0.4, 0.3, 0.2, 0.1], dtype=torch.float32, device=dev)
+    work = torch.empty(4 * 1024, dtype=torch.float32, device=dev)
+
+    def call(i):
+        w = ws[i % copies]
+        if args.op == "qkv":
+            q.rmsnorm_qgemv(w[0], x, g1, eps, y=y[:6144])
+        elif args.op == "o_proj":
+            q.qgemv_w4g64(w[0], x, y=y[:H], residual=x)
+        elif args.op == "swiglu":
+            q.swiglu_qgemv(w[0], w[1], x, g2, eps, h=y[:I])
+        elif args.op == "down":
+            q.qgemv_w4g64(w[0], xi, y=y[:H], residual=x)
+        else:
+            q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y[:H], workspace=work)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(copies):
+            call(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(copies):
+            call(i)
+    reps = max(1, args.steps // copies)
+    for _ in range(max(3, args.warmup // copies)):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * copies)
+    peak, peak_kind = measured_peak()
+    print(json.dumps({"op": args.op, "metric": "achieved HBM GB/s of one op (CUDA-graph replays)",
+                      "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                      "us_per_launch": round(ms * 1e3, 3), "bytes_per_launch": nbytes,
+                      "weight_copies": copies, "launches_timed": reps * copies, "peak": peak,
+                      "peak_kind": peak_kind, "device_status": q.device_status()}), flush=True)
     return 0
 
 
@@ -482,6 +592,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op != "stack":
+        return run_op(args)
     return run_own(args)
 
 

@@ -52,9 +52,8 @@ struct StreamPlan {
   bool ok = false;
   int ub = 0, tg = 0, t = 0, s = 0, jr = 0, rs = 0, ns = 0, stage_bytes = 0, grid = 0;
   int red_bytes = 0;   // partial-sum slots per stage
-  int x_bytes = 0;     // activations (fp16 pairs) and their unit sums
   int interleave = 0;  // 1: CTAs take stages round-robin
-  int smem_bytes = 0;  // dynamic shared memory: ns * (stage_bytes + red_bytes) + x_bytes
+  int smem_bytes = 0;  // dynamic shared memory: ns * (stage_bytes + red_bytes)
 };
 
 // Choose the thread counts, tasks per thread, rows per stage and ring depth
@@ -93,9 +92,9 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   const long long stage = static_cast<long long>(tasks) * task_bytes;
   if (stage > 100 * 1024) return p;
   const int red = ((tasks * (tg / 32) + 3) & ~3) * static_cast<int>(sizeof(float));
-  const int nvec = (mode == kMoeDown) ? top_k : 1;
-  const int xb = nvec * (K * 2 + (K / kSliceK) * static_cast<int>(sizeof(float)));
-  int ns = static_cast<int>((ring_budget - xb) / (stage + red));
+  // (activations are held in registers, loaded straight from global memory:
+  // shared memory is all ring)
+  int ns = static_cast<int>(ring_budget / (stage + red));
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) return p;
   p.ok = true;
@@ -108,8 +107,7 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   p.ns = ns;
   p.stage_bytes = static_cast<int>(stage);
   p.red_bytes = red;
-  p.x_bytes = xb;
-  p.smem_bytes = ns * (static_cast<int>(stage) + red) + xb;
+  p.smem_bytes = ns * (static_cast<int>(stage) + red);
   p.grid = static_cast<int>(rows < sms ? rows : sms);
   // Interleave stages across CTAs when that keeps the SMs within one stage
   // of each other (and, for kMoeUp, stages never straddle experts).

@@ -33,9 +33,12 @@
 //    computed (rows past the stage's end read stale but valid shared memory)
 //    and masked afterwards, so the compiler can interleave the rows' FMA
 //    chains and hoist their shared-memory loads.
+//  * Every thread loads its own 32-k activation slice straight from global
+//    memory (L2): no block-wide staging, so no barrier among the consumer
+//    warps at all, and each starts as soon as its slice and stage are in.
 //  * Every mbarrier wait is bounded (about 1 s); a timeout sets a status bit
-//    and the waiting thread returns instead of hanging (no named barrier is
-//    entered after the first wait, so nothing is left waiting).
+//    and the waiting thread returns instead of hanging (no named barrier
+//    exists, so nothing is left waiting).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -153,6 +156,84 @@ __device__ __forceinline__ float slice_dot(const uint8_t* codes, const unsigned 
   return fmaf(s, t, b * xs_scaled);
 }
 
+// A thread's 32 activations k in [k0, k0 + 32), read straight from global
+// memory: fp16 x (times gamma when given) or fp32 xf, rounded to fp16 once
+// (the kernels multiply fp16 activations), one value per 16-bit register,
+// and their sum times 2^-24 (the dot products' scale).  16-byte aligned.
+__device__ __forceinline__ void load_slice(const __half* x, const __half* gamma, const float* xf,
+                                           int k0, unsigned short (&xr)[kSliceK],
+                                           float& xs_scaled) {
+  float xv[kSliceK];
+  if (xf != nullptr) {
+    const float4* src = reinterpret_cast<const float4*>(xf + k0);
+#pragma unroll
+    for (int i = 0; i < kSliceK / 4; ++i) {
+      const float4 f = src[i];
+      xv[4 * i + 0] = f.x;
+      xv[4 * i + 1] = f.y;
+      xv[4 * i + 2] = f.z;
+      xv[4 * i + 3] = f.w;
+    }
+  } else {
+    uint4 raw[kSliceK / 8], graw[kSliceK / 8];
+#pragma unroll
+    for (int i = 0; i < kSliceK / 8; ++i) raw[i] = reinterpret_cast<const uint4*>(x + k0)[i];
+    if (gamma != nullptr) {
+#pragma unroll
+      for (int i = 0; i < kSliceK / 8; ++i) graw[i] = reinterpret_cast<const uint4*>(gamma + k0)[i];
+    }
+#pragma unroll
+    for (int i = 0; i < kSliceK / 8; ++i) {
+      const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(h[j]);
+        xv[8 * i + 2 * j] = f.x;
+        xv[8 * i + 2 * j + 1] = f.y;
+      }
+      if (gamma != nullptr) {
+        const __half2* g = reinterpret_cast<const __half2*>(&graw[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(g[j]);
+          xv[8 * i + 2 * j] *= f.x;
+          xv[8 * i + 2 * j + 1] *= f.y;
+        }
+      }
+    }
+  }
+  float part[kSliceK / 8];
+#pragma unroll
+  for (int i = 0; i < kSliceK / 8; ++i) part[i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSliceK; ++k) {
+    const __half h = __float2half_rn(xv[k]);
+    xr[k] = __half_as_ushort(h);
+    part[k / 8] += __half2float(h);
+  }
+  xs_scaled = ((part[0] + part[1]) + (part[2] + part[3])) * kTwoM24;
+}
+
+// 1 / sqrt(mean(x^2) + eps) of an fp16 vector of length K (a multiple of
+// 256), computed by one warp with 16-byte loads; every lane returns it.
+__device__ __forceinline__ float warp_rstd(const __half* x, int K, float eps, int lane) {
+  float sq = 0.f;
+  const uint4* v = reinterpret_cast<const uint4*>(x);
+#pragma unroll 4
+  for (int i = lane; i < K / 8; i += 32) {
+    const uint4 raw = v[i];
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(h[j]);
+      sq = fmaf(f.x, f.x, fmaf(f.y, f.y, sq));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  return 1.0f / sqrtf(sq / static_cast<float>(K) + eps);
+}
+
 template <int BITS, int MODE, int JR>
 __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   using SL = Slice<BITS>;
@@ -161,7 +242,6 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t part_bar[kMaxStages];
-  __shared__ float s_norm[17];
   __shared__ int s_eidx[kMaxTopK];
   __shared__ float s_ewt[kMaxTopK];
 
@@ -265,88 +345,15 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   const int wpt = TG >> 5;       // warps per slot
   const int ek = (MODE == kMoeDown) ? slot % a.top_k : 0;  // kMoeDown: fixed expert slot
   const bool use_gamma = (MODE == kNorm) || (MODE == kSwiglu && a.gamma != nullptr);
-  const int nwarps = T / 32;
   const int tasks = MS * a.RS;  // per stage
   // Per-stage partial-sum slots, after the ring: [NS][tasks][wpt].
   float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(NS) * a.stage_bytes);
   const int red_stage = (tasks * wpt + 3) & ~3;  // floats, 16-byte multiple
 
-  // Activations, converted once per CTA into shared memory (after the ring
-  // and the partial-sum slots): fp16 in k order, and the fp32 sum of every
-  // 32-k slice.  kMoeDown keeps one vector per expert slot.
-  const int nvec = (MODE == kMoeDown) ? a.top_k : 1;
-  const int spv = a.K / kSliceK;  // slices per vector
-  __half* x_sm = reinterpret_cast<__half*>(red + static_cast<size_t>(NS) * red_stage);
-  float* xsum_sm = reinterpret_cast<float*>(x_sm + static_cast<size_t>(nvec) * a.K);
-  float sq = 0.f;
-  // One group of 8 activations per thread and trip; 4 lanes make a slice.
-  for (int gi = t; !epi && gi < nvec * a.K / 8; gi += T) {  // lane-uniform trip count
-    const int v = gi / (a.K / 8);
-    const int k0 = (gi - v * (a.K / 8)) * 8;
-    float xv[8];
-    if (MODE == kMoeDown) {
-      const float4* src = reinterpret_cast<const float4*>(a.xf + static_cast<size_t>(v) * a.K + k0);
-      const float4 f0 = src[0], f1 = src[1];
-      xv[0] = f0.x;
-      xv[1] = f0.y;
-      xv[2] = f0.z;
-      xv[3] = f0.w;
-      xv[4] = f1.x;
-      xv[5] = f1.y;
-      xv[6] = f1.z;
-      xv[7] = f1.w;
-    } else {
-      const uint4 raw = *reinterpret_cast<const uint4*>(a.x + k0);
-      const __half2* h = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(h[j]);
-        xv[2 * j] = f.x;
-        xv[2 * j + 1] = f.y;
-        sq = fmaf(f.x, f.x, fmaf(f.y, f.y, sq));
-      }
-      if (use_gamma) {
-        const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + k0);
-        const __half2* g = reinterpret_cast<const __half2*>(&graw);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(g[j]);
-          xv[2 * j] *= f.x;
-          xv[2 * j + 1] *= f.y;
-        }
-      }
-    }
-    // Round to fp16 once (the kernel multiplies fp16 activations).
-    uint4 packed;
-    uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
-    float part = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half lo = __float2half_rn(xv[2 * j]), hi = __float2half_rn(xv[2 * j + 1]);
-      pw[j] = pack_half2(lo, hi);
-      part += __half2float(lo) + __half2float(hi);
-    }
-    *reinterpret_cast<uint4*>(x_sm + static_cast<size_t>(gi) * 8) = packed;
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    if ((lane & 3) == 0) xsum_sm[gi / 4] = part;
-  }
-  float rstd = 1.f;
-  if (use_gamma && !epi) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) s_norm[warp - 2] = sq;
-  }
-  // The only barrier among consumers and the epilogue warp; it runs before
-  // any mbarrier wait.
-  named_bar_sync(1, T + 32);
-  if (use_gamma) {
-    float tot = 0.f;
-    for (int w = 0; w < nwarps; ++w) tot += s_norm[w];
-    rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
-  }
   if (epi) {
-    // Epilogue warp: finish every stage's rows once all partials are in.
+    // Epilogue warp: RMS of the input (RMSNorm modes), then finish every
+    // stage's rows once all partials are in.
+    const float rstd = use_gamma ? warp_rstd(a.x, a.K, a.eps, lane) : 1.f;
     for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
       const int n = wk.rows();
       const int s = wk.slot;
@@ -394,23 +401,15 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   }
 
   // This thread's 32 activations, one fp16 per register, and their sum
-  // (times 2^-24, the dot products' scale).
+  // (times 2^-24, the dot products' scale), straight from global memory:
+  // no block-wide staging or barrier, so each warp starts on its own.
   unsigned short xr[kSliceK];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(x_sm + static_cast<size_t>(ek) * a.K +
-                                                      static_cast<size_t>(uu) * kSliceK);
-#pragma unroll
-    for (int i = 0; i < kSliceK / 8; ++i) {
-      const uint4 v = src[i];
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        xr[8 * i + 2 * j] = static_cast<unsigned short>(w4[j] & 0xffffu);
-        xr[8 * i + 2 * j + 1] = static_cast<unsigned short>(w4[j] >> 16);
-      }
-    }
-  }
-  const float xs_scaled = xsum_sm[ek * spv + uu] * kTwoM24;
+  float xs_scaled;
+  if (MODE == kMoeDown)
+    load_slice(nullptr, nullptr, a.xf + static_cast<size_t>(ek) * a.K, uu * kSliceK, xr,
+               xs_scaled);
+  else
+    load_slice(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * kSliceK, xr, xs_scaled);
   const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
   const int group_in_row = (uu * kSliceK) / 64;
   // Task j of this thread in every stage: matrix slot and row, and the

@@ -15,11 +15,14 @@
 // part of the token.  Here the producer warp of every CTA streams the
 // weights of all ops of all layers back to back through one TMA ring
 // (weights never depend on activations), so the ring stays full across op
-// boundaries.  Only the consumers of an op wait, on a grid-wide counter, for
-// the op that produces their input; the epilogue warp publishes each op's
-// completion (fence + atomic).  The launch is cooperative, so every CTA is
-// resident and the counter waits can always complete; each wait is bounded
-// (~1 s) and sets the library status bit instead of hanging.
+// boundaries.  Only the consumers of an op wait for the op that produces
+// their input: the epilogue warp publishes each op's completion on a
+// grid-wide counter (fence + atomic), one lane per CTA polls that counter
+// (acquire) and passes it on to the CTA's consumer warps through a
+// shared-memory mbarrier, and each consumer thread then loads its own
+// 32-k input slice from global memory.  The launch is cooperative, so every
+// CTA is resident and the counter waits can always complete; each wait is
+// bounded (~1 s) and sets the library status bit instead of hanging.
 #include <atomic>
 
 #include "qgemv.h"
@@ -53,7 +56,7 @@ struct StackArgs {
   __half* h;
   __half* act;
   __half* xbuf[2];
-  int* counters;  // [n_layers][4], zero on entry
+  int* counters;  // [n_layers * 4] lines of 128 bytes, zero on entry
   int n_layers, H, n_q, n_kv, hd, I;
   float eps;
   int NS, slot_bytes, red_slot_floats;
@@ -117,6 +120,13 @@ __device__ bool wait_counter(const int* c, int target) {
   }
 }
 
+// Grid completion counter of op c; each on its own 128-byte line, so the
+// pollers of one op and the adders of the next do not share a line.
+constexpr int kCounterStride = 32;
+__device__ __forceinline__ int* counter(const StackArgs& a, int c) {
+  return a.counters + c * kCounterStride;
+}
+
 __device__ __forceinline__ const __half* op_input(const StackArgs& a, int l, int k) {
   switch (k) {
     case 0: return l == 0 ? a.x_in : a.xbuf[l & 1];
@@ -136,7 +146,10 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t part_bar[kMaxStages];
-  __shared__ int s_abort;
+  // One phase per op: the epilogue warp's lane 0 acquires the grid counter of
+  // the op's input and arrives here; the consumer warps wait here instead of
+  // all polling the counter.
+  __shared__ __align__(8) uint64_t dep_bar;
 
   const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
@@ -145,18 +158,17 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
   const int P = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    s_abort = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&part_bar[s]), static_cast<uint32_t>(T / 32));
       mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32 + 1));
     }
+    mbar_init(smem_u32(&dep_bar), 1);
     fence_mbar_init();
   }
   __syncthreads();
 
   float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(NS) * a.slot_bytes);
-  __half* x_sm = reinterpret_cast<__half*>(red + static_cast<size_t>(NS) * a.red_slot_floats);
 
   // ------------------------------------------------------------ producer
   if (warp == 0) {
@@ -210,22 +222,23 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
       for (int k = 0; k < kOps; ++k) {
         const OpPlanDev& p = a.plan[k];
         const int dep = dependency(l, k);
-        // Every lane acquires the producing op's completion itself.
-        const int ok = (dep >= 0) ? wait_counter(a.counters + dep, P) : 1;
-        if (!__all_sync(0xffffffffu, ok)) return;
-        // RMS of the op's normalised input (ops 0 and 2).
-        float rstd = 1.f;
-        if (k == 0 || k == 2) {
-          const __half* xin = (k == 0) ? layer_input(a, l) : a.h;
-          float sq = 0.f;
-          for (int i = lane; i < a.H; i += 32) {
-            const float v = __half2float(xin[i]);
-            sq = fmaf(v, v, sq);
-          }
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-          rstd = 1.0f / sqrtf(sq / static_cast<float>(a.H) + a.eps);
+        // Lane 0 acquires the producing op's completion (gpu scope), then
+        // passes it on to this warp (__syncwarp) and to the consumer warps
+        // (the dependency barrier's release/acquire).  On a timeout nothing
+        // arrives and the consumers' own bounded wait ends them.
+        int ok = 1;
+        if (lane == 0 && dep >= 0) {
+          ok = wait_counter(counter(a, dep), P);
+          __threadfence();
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&dep_bar));
+        // RMS of the op's normalised input (ops 0 and 2).
+        const float rstd = (k == 0)   ? warp_rstd(layer_input(a, l), a.H, a.eps, lane)
+                           : (k == 2) ? warp_rstd(a.h, a.H, a.eps, lane)
+                                      : 1.f;
         const int wpt = p.TG >> 5;
         const OpRows o = op_rows(p);
         __half* out = (k == 0) ? a.qkv
@@ -263,7 +276,7 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
         // This CTA's rows of op (l, k) are written: publish.
         __threadfence();
         __syncwarp();
-        if (lane == 0) atomicAdd(a.counters + l * kOps + k, 1);
+        if (lane == 0) atomicAdd(counter(a, l * kOps + k), 1);
       }
     }
     return;
@@ -276,67 +289,8 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
     const StackLayerDev& L = a.layers[l];
     for (int k = 0; k < kOps; ++k) {
       const OpPlanDev& p = a.plan[k];
-      const int dep = dependency(l, k);
-      // Input ready everywhere, and every consumer done with the previous op.
-      if (dep >= 0 && t == 0) {
-        if (!wait_counter(a.counters + dep, P)) s_abort = 1;
-        __threadfence();
-      }
-      named_bar_sync(2, T);
-      if (*reinterpret_cast<volatile int*>(&s_abort) != 0) return;
-
-      // Convert the op's input into shared memory (fp16 in k order) and
-      // sum each 32-k slice.  ops 0 and 2 multiply by gamma here; rstd is
-      // applied by the epilogue warp.  op 1 gathers the value heads.
-      const int K = p.K;
-      const __half* gam = (k == 0) ? L.g1 : (k == 2) ? L.g2 : nullptr;
-      float* xsum_sm = reinterpret_cast<float*>(x_sm + K);
-      for (int gi = t; gi < K / 8; gi += T) {  // lane-uniform trip count
-        const int k0 = gi * 8;
-        const __half* src;
-        if (k == 1) {
-          const int head = k0 / a.hd;
-          src = a.qkv + static_cast<long long>(a.n_q + a.n_kv + head / (a.n_q / a.n_kv)) * a.hd +
-                (k0 - head * a.hd);
-        } else {
-          src = op_input(a, l, k) + k0;
-        }
-        const uint4 raw = *reinterpret_cast<const uint4*>(src);
-        const __half2* hv = reinterpret_cast<const __half2*>(&raw);
-        float xv[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(hv[j]);
-          xv[2 * j] = f.x;
-          xv[2 * j + 1] = f.y;
-        }
-        if (gam != nullptr) {
-          const uint4 graw = *reinterpret_cast<const uint4*>(gam + k0);
-          const __half2* gv = reinterpret_cast<const __half2*>(&graw);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(gv[j]);
-            xv[2 * j] *= f.x;
-            xv[2 * j + 1] *= f.y;
-          }
-        }
-        uint4 packed;
-        uint32_t* pw = reinterpret_cast<uint32_t*>(&packed);
-        float part = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __half lo = __float2half_rn(xv[2 * j]), hi = __float2half_rn(xv[2 * j + 1]);
-          pw[j] = pack_half2(lo, hi);
-          part += __half2float(lo) + __half2float(hi);
-        }
-        *reinterpret_cast<uint4*>(x_sm + k0) = packed;
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if ((lane & 3) == 0) xsum_sm[gi / 4] = part;
-      }
-      named_bar_sync(2, T);
-
       // This op's thread mapping.
+      const int K = p.K;
       const int TG = p.TG, S = p.S;
       const bool active = t < S * TG;  // whole warps
       const int slot = active ? t / TG : 0;
@@ -345,23 +299,30 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
       const int rcb = K / 2, rgb = K / 32;
       const int scales_off = p.MS * p.RS * rcb;
       const int biases_off = scales_off + p.MS * p.RS * rgb;
+      // Input ready everywhere (the epilogue warp has acquired it); then each
+      // thread loads its own 32-k slice of the input straight from global
+      // memory.  ops 0 and 2 multiply by gamma here; rstd is applied by the
+      // epilogue warp.
+      if (!mbar_wait(smem_u32(&dep_bar), static_cast<uint32_t>(l * kOps + k) & 1u, &g_status))
+        return;
       unsigned short xr[kSliceK];
       float xs_scaled = 0.f;
-      int task_row[JR], code_off[JR], group_off[JR];
       if (active) {
-        const uint4* src = reinterpret_cast<const uint4*>(x_sm + uu * kSliceK);
-#pragma unroll
-        for (int i = 0; i < kSliceK / 8; ++i) {
-          const uint4 v = src[i];
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            xr[8 * i + 2 * j] = static_cast<unsigned short>(w4[j] & 0xffffu);
-            xr[8 * i + 2 * j + 1] = static_cast<unsigned short>(w4[j] >> 16);
-          }
+        const int k0 = uu * kSliceK;
+        if (k == 1) {
+          // attention output = the value heads of qkv; a 32-k slice lies
+          // inside one head (head_dim % 32 == 0)
+          const int head = k0 / a.hd;
+          const __half* src = a.qkv +
+                              static_cast<long long>(a.n_q + a.n_kv + head / (a.n_q / a.n_kv)) * a.hd +
+                              (k0 - head * a.hd);
+          load_slice(src, nullptr, nullptr, 0, xr, xs_scaled);
+        } else {
+          const __half* gam = (k == 0) ? L.g1 : (k == 2) ? L.g2 : nullptr;
+          load_slice(op_input(a, l, k), gam, nullptr, k0, xr, xs_scaled);
         }
-        xs_scaled = xsum_sm[uu] * kTwoM24;
       }
+      int task_row[JR], code_off[JR], group_off[JR];
       const int group_in_row = (uu * kSliceK) / 64;
 #pragma unroll
       for (int j = 0; j < JR; ++j) {
@@ -417,7 +378,7 @@ size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape* shape) {
   if (shape == nullptr || shape->n_layers < 1) return 0;
   auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
   const size_t nqkv = static_cast<size_t>(shape->n_q + 2 * shape->n_kv) * shape->head_dim;
-  return up(sizeof(int) * 4 * static_cast<size_t>(shape->n_layers)) + up(2 * nqkv) +
+  return up(128 * 4 * static_cast<size_t>(shape->n_layers)) + up(2 * nqkv) +
          up(2 * static_cast<size_t>(shape->hidden)) + up(2 * static_cast<size_t>(shape->inter)) +
          2 * up(2 * static_cast<size_t>(shape->hidden));
 }
@@ -429,8 +390,8 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   if (!layers || !shape || !x || !y || !workspace) return QGEMV_ENULL;
   const int H = shape->hidden, nq = shape->n_q, nkv = shape->n_kv, hd = shape->head_dim;
   const int I = shape->inter, NL = shape->n_layers;
-  if (NL < 1 || NL > kMaxStackLayers || nq < 1 || nkv < 1 || nq % nkv != 0 || hd < 8 ||
-      hd % 8 != 0 || !(shape->eps > 0.0f))
+  if (NL < 1 || NL > kMaxStackLayers || nq < 1 || nkv < 1 || nq % nkv != 0 || hd < 32 ||
+      hd % 32 != 0 || !(shape->eps > 0.0f))
     return QGEMV_EINVAL;
   const int Dq = nq * hd;
   const int nqkv = (nq + 2 * nkv) * hd;
@@ -467,7 +428,7 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   const int kinds[kOps] = {kNorm, kPlain, kSwiglu, kPlain};
   const int Ks[kOps] = {H, Dq, H, I};
   const int rows[kOps] = {nqkv, H, I, H};
-  int slot_bytes = 0, red_floats = 0, x_bytes = 0;
+  int slot_bytes = 0, red_floats = 0;
   for (int k = 0; k < kOps; ++k) {
     const StreamPlan p = make_stream_plan(kinds[k], 4, Ks[k], rows[k], 1, sms, 512, kStackJR);
     if (!p.ok || p.jr != kStackJR) return QGEMV_EINVAL;
@@ -483,22 +444,20 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
     slot_bytes = slot_bytes > p.stage_bytes ? slot_bytes : p.stage_bytes;
     const int rf = ((p.s * p.jr * (p.tg / 32)) + 3) & ~3;
     red_floats = red_floats > rf ? red_floats : rf;
-    const int xb = Ks[k] * 2 + (Ks[k] / kSliceK) * 4;
-    x_bytes = x_bytes > xb ? x_bytes : xb;
   }
-  int ns = (200 * 1024 - x_bytes) / (slot_bytes + red_floats * 4);
+  int ns = (200 * 1024) / (slot_bytes + red_floats * 4);
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) return QGEMV_EINVAL;
   a.NS = ns;
   a.slot_bytes = slot_bytes;
   a.red_slot_floats = red_floats;
-  const int smem = ns * (slot_bytes + red_floats * 4) + x_bytes;
+  const int smem = ns * (slot_bytes + red_floats * 4);
 
   // Workspace: counters, qkv, h, act, x ping-pong.
   auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
   uint8_t* wp = static_cast<uint8_t*>(workspace);
   a.counters = reinterpret_cast<int*>(wp);
-  wp += up(sizeof(int) * 4 * static_cast<size_t>(NL));
+  wp += up(128 * 4 * static_cast<size_t>(NL));
   a.qkv = reinterpret_cast<__half*>(wp);
   wp += up(2 * static_cast<size_t>(nqkv));
   a.h = reinterpret_cast<__half*>(wp);
@@ -530,7 +489,7 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 576, smem) != cudaSuccess ||
       per_sm < 1)
     return QGEMV_ELAUNCH;
-  if (cudaMemsetAsync(a.counters, 0, sizeof(int) * 4 * static_cast<size_t>(NL), st) != cudaSuccess)
+  if (cudaMemsetAsync(a.counters, 0, 128 * 4 * static_cast<size_t>(NL), st) != cudaSuccess)
     return QGEMV_ELAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms));

@@ -236,7 +236,7 @@ size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape *shape);
  * device (16-byte aligned, may not overlap the workspace); workspace:
  * device, 256-byte aligned, >= qgemv_decode_stack_workspace_bytes bytes,
  * contents on entry ignored.  Checks: 1 <= n_layers <= 64, n_q % n_kv == 0,
- * head_dim % 8 == 0, hidden, n_q*head_dim and inter multiples of 1024 and at
+ * head_dim % 32 == 0, hidden, n_q*head_dim and inter multiples of 1024 and at
  * most 16384, eps > 0.  Enqueues a memset of the workspace's counters and
  * one cooperative launch on `stream`.
  */
