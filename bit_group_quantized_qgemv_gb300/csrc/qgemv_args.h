@@ -18,7 +18,7 @@ enum Mode : int {
 };
 
 constexpr int kMaxStages = 16;
-constexpr int kSliceK = 32;  // k values of a row one streaming-kernel thread owns
+constexpr int kSliceK = 32;  // smallest k range of a row one streaming-kernel thread owns
 constexpr int kMaxTopK = 8;
 constexpr int kMaxM = 8;
 
@@ -50,6 +50,7 @@ struct StreamArgs {
 
 struct StreamPlan {
   bool ok = false;
+  int kpt = 0;  // k per thread and task (32: half a quantisation group)
   int ub = 0, tg = 0, t = 0, s = 0, jr = 0, rs = 0, ns = 0, stage_bytes = 0, grid = 0;
   int red_bytes = 0;   // partial-sum slots per stage
   int interleave = 0;  // 1: CTAs take stages round-robin
@@ -59,7 +60,7 @@ struct StreamPlan {
 // Choose the thread counts, tasks per thread, rows per stage and ring depth
 // of the streaming kernel.  ok = false when it does not apply (the generic
 // kernel runs instead): K must be a multiple of 1024 and at most 16384, so
-// that a row's TG = K/32 slices span whole warps and every scale row is a
+// that a row's TG = K/KPT tasks span whole warps and every scale row is a
 // multiple of 16 bytes.
 inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, int top_k,
                                    int sms, int target_threads = 512, int max_jr = 4,
@@ -68,7 +69,8 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   StreamPlan p;
   if ((bits != 4 && bits != 2) || K % 1024 != 0 || K / kSliceK > 512 || rows <= 0 || sms <= 0)
     return p;
-  const int tg = K / kSliceK;
+  const int kpt = kSliceK;
+  const int tg = K / kpt;
   int s;
   if (mode == kMoeDown) {
     if (top_k < 1 || top_k > kMaxTopK || tg * top_k > 512) return p;
@@ -98,7 +100,8 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns < 2) return p;
   p.ok = true;
-  p.ub = kSliceK * bits / 8;
+  p.kpt = kpt;
+  p.ub = kpt * bits / 8;
   p.tg = tg;
   p.t = t;
   p.s = s;

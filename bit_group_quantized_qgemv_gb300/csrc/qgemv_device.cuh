@@ -132,13 +132,16 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 // fma(q, scale*x, bias*x) form of the FMA-reordered dequantisation,
 // factored over the 64 k of a group.
 //
-// x[j] is the fp16 activation of k = 8i + j, one per 16-bit register, so no
-// instruction is spent taking halves of packed registers apart.
-__device__ __forceinline__ void dot_word4(uint32_t w, const unsigned short* x, float& a,
-                                          float& b) {
+// The activations come packed in the same pairing as the code lanes:
+// xp[j] = (x_{8i+j}, x_{8i+j+4}) for j = 0..3 (low half first), so every
+// fma pairs the low (high) half of a code register with the low (high) half
+// of an activation register; the fma reads either half directly, so no
+// instruction unpacks anything.
+__device__ __forceinline__ void dot_word4(uint32_t w, const uint32_t* xp, float& a, float& b) {
   asm("{\n"
       ".reg .b32 v0, v1, v2, v3, w8;\n"
       ".reg .b16 q0, q1, q2, q3, q4, q5, q6, q7;\n"
+      ".reg .b16 x0, x1, x2, x3, x4, x5, x6, x7;\n"
       "and.b32 v0, %2, 0x000F000F;\n"
       "and.b32 v1, %2, 0x00F000F0;\n"
       "shr.u32 w8, %2, 8;\n"
@@ -148,31 +151,35 @@ __device__ __forceinline__ void dot_word4(uint32_t w, const unsigned short* x, f
       "mov.b32 {q1, q5}, v1;\n"
       "mov.b32 {q2, q6}, v2;\n"
       "mov.b32 {q3, q7}, v3;\n"
-      "fma.rn.f32.f16 %0, q0, %3, %0;\n"
-      "fma.rn.f32.f16 %1, q1, %4, %1;\n"
-      "fma.rn.f32.f16 %0, q4, %7, %0;\n"
-      "fma.rn.f32.f16 %1, q5, %8, %1;\n"
-      "fma.rn.f32.f16 %0, q2, %5, %0;\n"
-      "fma.rn.f32.f16 %1, q3, %6, %1;\n"
-      "fma.rn.f32.f16 %0, q6, %9, %0;\n"
-      "fma.rn.f32.f16 %1, q7, %10, %1;\n"
+      "mov.b32 {x0, x4}, %3;\n"
+      "mov.b32 {x1, x5}, %4;\n"
+      "mov.b32 {x2, x6}, %5;\n"
+      "mov.b32 {x3, x7}, %6;\n"
+      "fma.rn.f32.f16 %0, q0, x0, %0;\n"
+      "fma.rn.f32.f16 %1, q1, x1, %1;\n"
+      "fma.rn.f32.f16 %0, q4, x4, %0;\n"
+      "fma.rn.f32.f16 %1, q5, x5, %1;\n"
+      "fma.rn.f32.f16 %0, q2, x2, %0;\n"
+      "fma.rn.f32.f16 %1, q3, x3, %1;\n"
+      "fma.rn.f32.f16 %0, q6, x6, %0;\n"
+      "fma.rn.f32.f16 %1, q7, x7, %1;\n"
       "}"
       : "+f"(a), "+f"(b)
-      : "r"(w), "h"(x[0]), "h"(x[1]), "h"(x[2]), "h"(x[3]), "h"(x[4]), "h"(x[5]), "h"(x[6]),
-        "h"(x[7]));
+      : "r"(w), "r"(xp[0]), "r"(xp[1]), "r"(xp[2]), "r"(xp[3]));
 }
 
 // A 2-bit word holds codes c_0..c_15 (k = 16i .. 16i+15), low bits first.
 // Masks 0x00030003, 0x000C000C, 0x00300030, 0x00C000C0 (on the word and on
-// the word >> 8) yield fp16 subnormals m * c * 2^-24 with m = 1, 4, 16, 64.
-// Class accumulators a (m=1), b (4), c (16), d (64):
-//   sum_k c_k x_k = (a + b / 4 + c / 16 + d / 64) * 2^24.
-// x[j] is the fp16 activation of k = 16i + j, one per 16-bit register.
-__device__ __forceinline__ void dot_word2(uint32_t w, const unsigned short* x, float& a, float& b,
+// the word >> 8) yield fp16 subnormals m * c * 2^-24 with m = 1, 4, 16, 64,
+// lane pairs (c_j, c_{j+8}).  Class accumulators a (m=1), b (4), c (16),
+// d (64):  sum_k c_k x_k = (a + b / 4 + c / 16 + d / 64) * 2^24.
+// Activations packed xp[j] = (x_{16i+j}, x_{16i+j+8}) for j = 0..7.
+__device__ __forceinline__ void dot_word2(uint32_t w, const uint32_t* xp, float& a, float& b,
                                           float& c, float& d) {
   asm("{\n"
       ".reg .b32 v0, v1, v2, v3, v4, v5, v6, v7, w8;\n"
       ".reg .b16 p0, p1, p2, p3, p4, p5, p6, p7, p8, p9, p10, p11, p12, p13, p14, p15;\n"
+      ".reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, x8, x9, x10, x11, x12, x13, x14, x15;\n"
       "and.b32 v0, %4, 0x00030003;\n"
       "and.b32 v1, %4, 0x000C000C;\n"
       "and.b32 v2, %4, 0x00300030;\n"
@@ -190,27 +197,34 @@ __device__ __forceinline__ void dot_word2(uint32_t w, const unsigned short* x, f
       "mov.b32 {p5, p13}, v5;\n"
       "mov.b32 {p6, p14}, v6;\n"
       "mov.b32 {p7, p15}, v7;\n"
-      "fma.rn.f32.f16 %0, p0, %5, %0;\n"
-      "fma.rn.f32.f16 %1, p1, %6, %1;\n"
-      "fma.rn.f32.f16 %2, p2, %7, %2;\n"
-      "fma.rn.f32.f16 %3, p3, %8, %3;\n"
-      "fma.rn.f32.f16 %0, p8, %13, %0;\n"
-      "fma.rn.f32.f16 %1, p9, %14, %1;\n"
-      "fma.rn.f32.f16 %2, p10, %15, %2;\n"
-      "fma.rn.f32.f16 %3, p11, %16, %3;\n"
-      "fma.rn.f32.f16 %0, p4, %9, %0;\n"
-      "fma.rn.f32.f16 %1, p5, %10, %1;\n"
-      "fma.rn.f32.f16 %2, p6, %11, %2;\n"
-      "fma.rn.f32.f16 %3, p7, %12, %3;\n"
-      "fma.rn.f32.f16 %0, p12, %17, %0;\n"
-      "fma.rn.f32.f16 %1, p13, %18, %1;\n"
-      "fma.rn.f32.f16 %2, p14, %19, %2;\n"
-      "fma.rn.f32.f16 %3, p15, %20, %3;\n"
+      "mov.b32 {x0, x8}, %5;\n"
+      "mov.b32 {x1, x9}, %6;\n"
+      "mov.b32 {x2, x10}, %7;\n"
+      "mov.b32 {x3, x11}, %8;\n"
+      "mov.b32 {x4, x12}, %9;\n"
+      "mov.b32 {x5, x13}, %10;\n"
+      "mov.b32 {x6, x14}, %11;\n"
+      "mov.b32 {x7, x15}, %12;\n"
+      "fma.rn.f32.f16 %0, p0, x0, %0;\n"
+      "fma.rn.f32.f16 %1, p1, x1, %1;\n"
+      "fma.rn.f32.f16 %2, p2, x2, %2;\n"
+      "fma.rn.f32.f16 %3, p3, x3, %3;\n"
+      "fma.rn.f32.f16 %0, p8, x8, %0;\n"
+      "fma.rn.f32.f16 %1, p9, x9, %1;\n"
+      "fma.rn.f32.f16 %2, p10, x10, %2;\n"
+      "fma.rn.f32.f16 %3, p11, x11, %3;\n"
+      "fma.rn.f32.f16 %0, p4, x4, %0;\n"
+      "fma.rn.f32.f16 %1, p5, x5, %1;\n"
+      "fma.rn.f32.f16 %2, p6, x6, %2;\n"
+      "fma.rn.f32.f16 %3, p7, x7, %3;\n"
+      "fma.rn.f32.f16 %0, p12, x12, %0;\n"
+      "fma.rn.f32.f16 %1, p13, x13, %1;\n"
+      "fma.rn.f32.f16 %2, p14, x14, %2;\n"
+      "fma.rn.f32.f16 %3, p15, x15, %3;\n"
       "}"
       : "+f"(a), "+f"(b), "+f"(c), "+f"(d)
-      : "r"(w), "h"(x[0]), "h"(x[1]), "h"(x[2]), "h"(x[3]), "h"(x[4]), "h"(x[5]), "h"(x[6]),
-        "h"(x[7]), "h"(x[8]), "h"(x[9]), "h"(x[10]), "h"(x[11]), "h"(x[12]), "h"(x[13]),
-        "h"(x[14]), "h"(x[15]));
+      : "r"(w), "r"(xp[0]), "r"(xp[1]), "r"(xp[2]), "r"(xp[3]), "r"(xp[4]), "r"(xp[5]),
+        "r"(xp[6]), "r"(xp[7]));
 }
 
 // Code q of k within a packed word (generic path).

@@ -13,9 +13,12 @@
 //    guarded by mbarriers.  No multicast.
 //  * The other T threads are consumers.  A stage holds MS x RS "tasks"
 //    (matrix slot, row).  Threads form slots of TG = K/32 threads; thread uu
-//    of a slot owns k in [32 uu, 32 uu + 32) of every row, so its 32
-//    activations sit in registers (one fp16 per register) for the whole
-//    kernel.  The S = T/TG slots take the tasks round-robin, JR per thread.
+//    of a slot owns k in [32 uu, 32 uu + 32) of every row (KPT = 32, half a
+//    quantisation group), so its activations sit in registers (16 packed
+//    fp16 pairs) for the whole kernel.  The S = T/TG slots take the tasks
+//    round-robin, JR per thread.  (Whole-group tasks, 64 k per thread,
+//    measured slower on GB300: twice the activation registers and 32-byte
+//    strided code loads.)
 //  * Inner loop: dot_word4 / dot_word2 (fp16-subnormal codes x fp16
 //    activations with the mixed fma.rn.f32.f16, exact products, fp32 sums),
 //    then scale * sum(q x) + bias * sum(x) per slice: the FMA-reordered
@@ -51,11 +54,13 @@ namespace qgemv {
 // Status word of this translation unit (bit kStatusWaitTimeout).
 static __device__ unsigned g_status = 0;
 
-template <int BITS>
-struct Slice {
-  static constexpr int kCodesPerWord = 32 / BITS;
-  static constexpr int kWords = kSliceK / kCodesPerWord;  // 4 (4-bit) or 2 (2-bit)
-  static constexpr int kBytes = kWords * 4;               // 16 or 8
+// A thread's task: KPT consecutive k of one row (KPT = 32: half a
+// quantisation group), its codes (KPT * BITS / 8 bytes) and its activations,
+// held as KPT / 2 packed fp16 pairs.
+template <int BITS, int KPT>
+struct Task {
+  static constexpr int kCodeBytes = KPT * BITS / 8;  // 16 / 32 (4-bit), 8 / 16 (2-bit)
+  static constexpr int kXRegs = KPT / 2;
 };
 
 // Stage walker shared by the producer, the consumers and the epilogue warp:
@@ -133,85 +138,108 @@ __device__ __forceinline__ float warp_reduce_rows(float (&v)[JR], int lane) {
   return r;
 }
 
-// One row slice: sum over its 32 k of w * x, in units of 2^-24.
-template <int BITS>
-__device__ __forceinline__ float slice_dot(const uint8_t* codes, const unsigned short* x, float s,
-                                           float b, float xs_scaled) {
+// One task: sum over its KPT k of w * x, in units of 2^-24, as
+// scale * sum(q x) + bias * sum(x) (xs_scaled = sum(x) * 2^-24).
+template <int BITS, int KPT>
+__device__ __forceinline__ float task_dot(const uint8_t* codes, const uint32_t* xp, float s,
+                                          float b, float xs_scaled) {
   float t;
   if (BITS == 4) {
-    const uint4 c = *reinterpret_cast<const uint4*>(codes);
-    float pa = 0.f, pb = 0.f, qa = 0.f, qb = 0.f;
-    dot_word4(c.x, x + 0, pa, pb);
-    dot_word4(c.y, x + 8, qa, qb);
-    dot_word4(c.z, x + 16, pa, pb);
-    dot_word4(c.w, x + 24, qa, qb);
-    t = fmaf(pb + qb, 0.0625f, pa + qa);
+    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < KPT / 32; ++q) {
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + 16 * q);
+      dot_word4(c.x, xp + 16 * q + 0, a0, b0);
+      dot_word4(c.y, xp + 16 * q + 4, a1, b1);
+      dot_word4(c.z, xp + 16 * q + 8, a0, b0);
+      dot_word4(c.w, xp + 16 * q + 12, a1, b1);
+    }
+    t = fmaf(b0 + b1, 0.0625f, a0 + a1);
   } else {
-    const uint2 c = *reinterpret_cast<const uint2*>(codes);
     float ca = 0.f, cb = 0.f, cc = 0.f, cd = 0.f;
-    dot_word2(c.x, x + 0, ca, cb, cc, cd);
-    dot_word2(c.y, x + 16, ca, cb, cc, cd);
+#pragma unroll
+    for (int q = 0; q < KPT / 32; ++q) {
+      const uint2 c = *reinterpret_cast<const uint2*>(codes + 8 * q);
+      dot_word2(c.x, xp + 16 * q + 0, ca, cb, cc, cd);
+      dot_word2(c.y, xp + 16 * q + 8, ca, cb, cc, cd);
+    }
     t = fmaf(cd, 0.015625f, fmaf(cc, 0.0625f, fmaf(cb, 0.25f, ca)));
   }
   return fmaf(s, t, b * xs_scaled);
 }
 
-// A thread's 32 activations k in [k0, k0 + 32), read straight from global
+// A thread's KPT activations k in [k0, k0 + KPT), read straight from global
 // memory: fp16 x (times gamma when given) or fp32 xf, rounded to fp16 once
-// (the kernels multiply fp16 activations), one value per 16-bit register,
-// and their sum times 2^-24 (the dot products' scale).  16-byte aligned.
-__device__ __forceinline__ void load_slice(const __half* x, const __half* gamma, const float* xf,
-                                           int k0, unsigned short (&xr)[kSliceK],
-                                           float& xs_scaled) {
-  float xv[kSliceK];
-  if (xf != nullptr) {
-    const float4* src = reinterpret_cast<const float4*>(xf + k0);
+// (the kernels multiply fp16 activations) and packed in the pairing of the
+// code lanes (4-bit: (x_{8i+j}, x_{8i+j+4}); 2-bit: (x_{16i+j}, x_{16i+j+8})),
+// plus their sum times 2^-24 (the dot products' scale).  16-byte aligned.
+template <int BITS, int KPT>
+__device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma, const float* xf,
+                                            int k0, uint32_t (&xp)[KPT / 2], float& xs_scaled) {
+  float part[KPT / 16];
 #pragma unroll
-    for (int i = 0; i < kSliceK / 4; ++i) {
-      const float4 f = src[i];
-      xv[4 * i + 0] = f.x;
-      xv[4 * i + 1] = f.y;
-      xv[4 * i + 2] = f.z;
-      xv[4 * i + 3] = f.w;
-    }
-  } else {
-    uint4 raw[kSliceK / 8], graw[kSliceK / 8];
+  for (int c = 0; c < KPT / 16; ++c) {  // 16 activations at a time
+    float xv[16];
+    if (xf != nullptr) {
+      const float4* src = reinterpret_cast<const float4*>(xf + k0 + 16 * c);
 #pragma unroll
-    for (int i = 0; i < kSliceK / 8; ++i) raw[i] = reinterpret_cast<const uint4*>(x + k0)[i];
-    if (gamma != nullptr) {
-#pragma unroll
-      for (int i = 0; i < kSliceK / 8; ++i) graw[i] = reinterpret_cast<const uint4*>(gamma + k0)[i];
-    }
-#pragma unroll
-    for (int i = 0; i < kSliceK / 8; ++i) {
-      const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(h[j]);
-        xv[8 * i + 2 * j] = f.x;
-        xv[8 * i + 2 * j + 1] = f.y;
+      for (int i = 0; i < 4; ++i) {
+        const float4 f = src[i];
+        xv[4 * i + 0] = f.x;
+        xv[4 * i + 1] = f.y;
+        xv[4 * i + 2] = f.z;
+        xv[4 * i + 3] = f.w;
       }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(x + k0 + 16 * c);
+      uint4 raw[2] = {src[0], src[1]};
+      uint4 graw[2];
       if (gamma != nullptr) {
-        const __half2* g = reinterpret_cast<const __half2*>(&graw[i]);
+        const uint4* g = reinterpret_cast<const uint4*>(gamma + k0 + 16 * c);
+        graw[0] = g[0];
+        graw[1] = g[1];
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const __half2* h = reinterpret_cast<const __half2*>(&raw[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(g[j]);
-          xv[8 * i + 2 * j] *= f.x;
-          xv[8 * i + 2 * j + 1] *= f.y;
+          float2 f = __half22float2(h[j]);
+          if (gamma != nullptr) {
+            const float2 gf = __half22float2(reinterpret_cast<const __half2*>(&graw[i])[j]);
+            f.x *= gf.x;
+            f.y *= gf.y;
+          }
+          xv[8 * i + 2 * j] = f.x;
+          xv[8 * i + 2 * j + 1] = f.y;
         }
       }
     }
-  }
-  float part[kSliceK / 8];
+    unsigned short hv[16];
+    part[c] = 0.f;
 #pragma unroll
-  for (int i = 0; i < kSliceK / 8; ++i) part[i] = 0.f;
+    for (int k = 0; k < 16; ++k) {
+      const __half h = __float2half_rn(xv[k]);
+      hv[k] = __half_as_ushort(h);
+      part[c] += __half2float(h);
+    }
+    if (BITS == 4) {
 #pragma unroll
-  for (int k = 0; k < kSliceK; ++k) {
-    const __half h = __float2half_rn(xv[k]);
-    xr[k] = __half_as_ushort(h);
-    part[k / 8] += __half2float(h);
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          xp[8 * c + 4 * i + j] = static_cast<uint32_t>(hv[8 * i + j]) |
+                                  (static_cast<uint32_t>(hv[8 * i + j + 4]) << 16);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        xp[8 * c + j] = static_cast<uint32_t>(hv[j]) | (static_cast<uint32_t>(hv[j + 8]) << 16);
+    }
   }
-  xs_scaled = ((part[0] + part[1]) + (part[2] + part[3])) * kTwoM24;
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < KPT / 16; ++c) sum += part[c];
+  xs_scaled = sum * kTwoM24;
 }
 
 // 1 / sqrt(mean(x^2) + eps) of an fp16 vector of length K (a multiple of
@@ -234,9 +262,9 @@ __device__ __forceinline__ float warp_rstd(const __half* x, int K, float eps, in
   return 1.0f / sqrtf(sq / static_cast<float>(K) + eps);
 }
 
-template <int BITS, int MODE, int JR>
+template <int BITS, int MODE, int JR, int KPT>
 __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
-  using SL = Slice<BITS>;
+  using TK = Task<BITS, KPT>;
   constexpr int NMAT = (MODE == kSwiglu || MODE == kMoeUp) ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -400,18 +428,18 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     return;
   }
 
-  // This thread's 32 activations, one fp16 per register, and their sum
-  // (times 2^-24, the dot products' scale), straight from global memory:
-  // no block-wide staging or barrier, so each warp starts on its own.
-  unsigned short xr[kSliceK];
+  // This thread's KPT activations, packed fp16 pairs, and their sum (times
+  // 2^-24, the dot products' scale), straight from global memory: no
+  // block-wide staging or barrier, so each warp starts on its own.
+  uint32_t xp[TK::kXRegs];
   float xs_scaled;
   if (MODE == kMoeDown)
-    load_slice(nullptr, nullptr, a.xf + static_cast<size_t>(ek) * a.K, uu * kSliceK, xr,
-               xs_scaled);
+    load_task_x<BITS, KPT>(nullptr, nullptr, a.xf + static_cast<size_t>(ek) * a.K, uu * KPT, xp,
+                           xs_scaled);
   else
-    load_slice(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * kSliceK, xr, xs_scaled);
+    load_task_x<BITS, KPT>(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * KPT, xp, xs_scaled);
   const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
-  const int group_in_row = (uu * kSliceK) / 64;
+  const int group_in_row = (uu * KPT) / 64;
   // Task j of this thread in every stage: matrix slot and row, and the
   // shared-memory offsets of its slice.
   int task_row[JR], code_off[JR], group_off[JR];
@@ -427,14 +455,13 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       rl = task - ms * a.RS;
     }
     task_row[j] = rl;
-    code_off[j] = (ms * a.RS + rl) * rcb + uu * SL::kBytes;
+    code_off[j] = (ms * a.RS + rl) * rcb + uu * TK::kCodeBytes;
     group_off[j] = (ms * a.RS + rl) * rgb + group_in_row * 2;
   }
 
   for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
     const int n = wk.rows();
     const int s = wk.slot;
-    const int row = wk.row;
     if (!mbar_wait(smem_u32(&full_bar[s]), wk.phase, &g_status)) return;
     const uint8_t* st = smem + static_cast<size_t>(s) * a.stage_bytes;
     bool slot_ok = expert_ok;
@@ -445,8 +472,8 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     for (int j = 0; j < JR; ++j) {
       const __half sv = *reinterpret_cast<const __half*>(st + scales_off + group_off[j]);
       const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
-      const float v = slice_dot<BITS>(st + codes_off + code_off[j], xr, __half2float(sv),
-                                      __half2float(bv), xs_scaled);
+      const float v = task_dot<BITS, KPT>(st + codes_off + code_off[j], xp, __half2float(sv),
+                                          __half2float(bv), xs_scaled);
       acc[j] = (task_row[j] < n && slot_ok) ? v : 0.f;
     }
 
@@ -477,11 +504,11 @@ inline cudaError_t ensure_smem_attr(F* kernel, int bytes, unsigned* done_mask, i
   return e;
 }
 
-template <int BITS, int MODE, int JR>
+template <int BITS, int MODE, int JR, int KPT>
 inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream_t stream,
                                    int device) {
   static unsigned done_mask = 0;
-  auto* k = stream_kernel<BITS, MODE, JR>;
+  auto* k = stream_kernel<BITS, MODE, JR, KPT>;
   cudaError_t e = ensure_smem_attr(k, 220 * 1024, &done_mask, device);
   if (e != cudaSuccess) return e;
   a.TG = p.tg;
@@ -499,10 +526,10 @@ template <int BITS, int MODE>
 inline cudaError_t launch_stream(const StreamPlan& p, const StreamArgs& a, cudaStream_t stream,
                                  int device) {
   switch (p.jr) {
-    case 8: return launch_stream_t<BITS, MODE, 8>(p, a, stream, device);
-    case 4: return launch_stream_t<BITS, MODE, 4>(p, a, stream, device);
-    case 2: return launch_stream_t<BITS, MODE, 2>(p, a, stream, device);
-    default: return launch_stream_t<BITS, MODE, 1>(p, a, stream, device);
+    case 8: return launch_stream_t<BITS, MODE, 8, 32>(p, a, stream, device);
+    case 4: return launch_stream_t<BITS, MODE, 4, 32>(p, a, stream, device);
+    case 2: return launch_stream_t<BITS, MODE, 2, 32>(p, a, stream, device);
+    default: return launch_stream_t<BITS, MODE, 1, 32>(p, a, stream, device);
   }
 }
 

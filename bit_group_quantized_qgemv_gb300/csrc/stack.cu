@@ -34,6 +34,7 @@ namespace {
 constexpr int kMaxStackLayers = 64;
 constexpr int kStackJR = 4;
 constexpr int kOps = 4;  // qkv, o, gate.up, down
+constexpr int kResRows = 256;  // residual rows an epilogue prefetches per op
 
 struct StackLayerDev {
   const uint8_t* w[5];  // qkv, o, gate, up, down codes
@@ -140,7 +141,87 @@ __device__ __forceinline__ const __half* layer_input(const StackArgs& a, int l) 
   return l == 0 ? a.x_in : a.xbuf[l & 1];
 }
 
-template <int JR>
+// The consumer warps' share of op (l, k): each thread loads its KPT-k slice
+// of the op's input straight from global memory (ops 0 and 2 multiply by
+// gamma here; rstd is applied by the epilogue warp), then streams the op's
+// stages from the ring.  Returns false after a timed-out wait.
+template <int KPT, int JR>
+__device__ __forceinline__ bool consume_op(const StackArgs& a, int l, int k, int t, int lane,
+                                           Ring& ring, uint8_t* smem, float* red,
+                                           uint64_t* full_bar, uint64_t* part_bar,
+                                           uint64_t* empty_bar) {
+  using TK = Task<4, KPT>;
+  const OpPlanDev& p = a.plan[k];
+  const StackLayerDev& L = a.layers[l];
+  const int K = p.K;
+  const int TG = p.TG, S = p.S;
+  const bool active = t < S * TG;  // whole warps
+  const int slot = active ? t / TG : 0;
+  const int uu = active ? t - slot * TG : 0;
+  const int wit = uu >> 5, wpt = TG >> 5;
+  const int rcb = K / 2, rgb = K / 32;
+  const int scales_off = p.MS * p.RS * rcb;
+  const int biases_off = scales_off + p.MS * p.RS * rgb;
+  uint32_t xp[TK::kXRegs];
+  float xs_scaled = 0.f;
+  if (active) {
+    const int k0 = uu * KPT;
+    if (k == 1) {
+      // attention output = the value heads of qkv; a 32-k slice lies
+      // inside one head (head_dim % 32 == 0, checked by the host)
+      const int head = k0 / a.hd;
+      const __half* src = a.qkv +
+                          static_cast<long long>(a.n_q + a.n_kv + head / (a.n_q / a.n_kv)) * a.hd +
+                          (k0 - head * a.hd);
+      load_task_x<4, KPT>(src, nullptr, nullptr, 0, xp, xs_scaled);
+    } else {
+      const __half* gam = (k == 0) ? L.g1 : (k == 2) ? L.g2 : nullptr;
+      load_task_x<4, KPT>(op_input(a, l, k), gam, nullptr, k0, xp, xs_scaled);
+    }
+  }
+  int task_row[JR], code_off[JR], group_off[JR];
+  const int group_in_row = (uu * KPT) / 64;
+#pragma unroll
+  for (int j = 0; j < JR; ++j) {
+    const int task = slot + j * S;
+    const int ms = task / p.RS;
+    const int rl = task - ms * p.RS;
+    task_row[j] = rl;
+    code_off[j] = (ms * p.RS + rl) * rcb + uu * TK::kCodeBytes;
+    group_off[j] = (ms * p.RS + rl) * rgb + group_in_row * 2;
+  }
+
+  const OpRows o = op_rows(p);
+  for (int row = o.r0; row < o.r1;) {
+    const int n = min(p.RS, o.r1 - row);
+    if (!mbar_wait(smem_u32(&full_bar[ring.slot]), ring.phase, &g_status)) return false;
+    if (active) {
+      const uint8_t* st = smem + static_cast<size_t>(ring.slot) * a.slot_bytes;
+      float acc[JR];
+#pragma unroll
+      for (int j = 0; j < JR; ++j) {
+        const __half sv = *reinterpret_cast<const __half*>(st + scales_off + group_off[j]);
+        const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
+        const float v = task_dot<4, KPT>(st + code_off[j], xp, __half2float(sv), __half2float(bv),
+                                         xs_scaled);
+        acc[j] = task_row[j] < n ? v : 0.f;
+      }
+      float* rs = red + static_cast<size_t>(ring.slot) * a.red_slot_floats;
+      constexpr int kLanesPerRow = 32 / JR;
+      const float v = warp_reduce_rows<JR>(acc, lane);
+      if ((lane & (kLanesPerRow - 1)) == 0) rs[(slot + (lane / kLanesPerRow) * S) * wpt + wit] = v;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&part_bar[ring.slot]));
+      mbar_arrive(smem_u32(&empty_bar[ring.slot]));
+    }
+    ring.advance();
+    row = next_row(o, row, n);
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ StackArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -150,6 +231,7 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
   // the op's input and arrives here; the consumer warps wait here instead of
   // all polling the counter.
   __shared__ __align__(8) uint64_t dep_bar;
+  __shared__ float res_sm[kResRows];  // epilogue: residual rows of the op
 
   const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
@@ -246,6 +328,24 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
                       : (k == 2) ? a.act
                                  : (l == a.n_layers - 1 ? a.y_out : a.xbuf[(l + 1) & 1]);
         const __half* resid = (k == 1) ? layer_input(a, l) : (k == 3) ? a.h : nullptr;
+        // Residual rows of ops 1 and 3 (complete: their producer op was
+        // acquired before), loaded all at once into shared memory so that the
+        // per-stage work needs no global round trip.  Row index = stage * RS +
+        // row in stage; rows past kResRows are read directly.
+        if (resid != nullptr) {
+          float rv[kResRows / 32];
+#pragma unroll
+          for (int i = 0; i < kResRows / 32; ++i) {
+            const int idx = lane + 32 * i;
+            const int g = idx / p.RS;
+            const int gr = o.stride ? o.r0 + g * o.stride + (idx - g * p.RS) : o.r0 + idx;
+            rv[i] = gr < o.r1 ? __half2float(resid[gr]) : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < kResRows / 32; ++i) res_sm[lane + 32 * i] = rv[i];
+          __syncwarp();
+        }
+        int sidx = 0;  // stage * RS
         for (int row = o.r0; row < o.r1;) {
           const int n = min(p.RS, o.r1 - row);
           if (!mbar_wait(smem_u32(&part_bar[ring.slot]), ring.phase, &g_status)) return;
@@ -264,7 +364,7 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
             } else if (k == 2) {
               res = silu_f(v0 * rstd) * (v1 * rstd);
             } else {
-              res = v0 + __half2float(resid[gr]);
+              res = v0 + (sidx + r < kResRows ? res_sm[sidx + r] : __half2float(resid[gr]));
             }
             out[gr] = __float2half_rn(res);
           }
@@ -272,6 +372,7 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[ring.slot]));
           ring.advance();
           row = next_row(o, row, n);
+          sidx += p.RS;
         }
         // This CTA's rows of op (l, k) are written: publish.
         __threadfence();
@@ -286,83 +387,14 @@ __global__ void __launch_bounds__(576, 1) stack_kernel(const __grid_constant__ S
   const int t = threadIdx.x - 64;
   Ring ring(NS);
   for (int l = 0; l < a.n_layers; ++l) {
-    const StackLayerDev& L = a.layers[l];
     for (int k = 0; k < kOps; ++k) {
       const OpPlanDev& p = a.plan[k];
-      // This op's thread mapping.
-      const int K = p.K;
-      const int TG = p.TG, S = p.S;
-      const bool active = t < S * TG;  // whole warps
-      const int slot = active ? t / TG : 0;
-      const int uu = active ? t - slot * TG : 0;
-      const int wit = uu >> 5, wpt = TG >> 5;
-      const int rcb = K / 2, rgb = K / 32;
-      const int scales_off = p.MS * p.RS * rcb;
-      const int biases_off = scales_off + p.MS * p.RS * rgb;
-      // Input ready everywhere (the epilogue warp has acquired it); then each
-      // thread loads its own 32-k slice of the input straight from global
-      // memory.  ops 0 and 2 multiply by gamma here; rstd is applied by the
-      // epilogue warp.
+      // Input ready everywhere: the epilogue warp has acquired it.
       if (!mbar_wait(smem_u32(&dep_bar), static_cast<uint32_t>(l * kOps + k) & 1u, &g_status))
         return;
-      unsigned short xr[kSliceK];
-      float xs_scaled = 0.f;
-      if (active) {
-        const int k0 = uu * kSliceK;
-        if (k == 1) {
-          // attention output = the value heads of qkv; a 32-k slice lies
-          // inside one head (head_dim % 32 == 0)
-          const int head = k0 / a.hd;
-          const __half* src = a.qkv +
-                              static_cast<long long>(a.n_q + a.n_kv + head / (a.n_q / a.n_kv)) * a.hd +
-                              (k0 - head * a.hd);
-          load_slice(src, nullptr, nullptr, 0, xr, xs_scaled);
-        } else {
-          const __half* gam = (k == 0) ? L.g1 : (k == 2) ? L.g2 : nullptr;
-          load_slice(op_input(a, l, k), gam, nullptr, k0, xr, xs_scaled);
-        }
-      }
-      int task_row[JR], code_off[JR], group_off[JR];
-      const int group_in_row = (uu * kSliceK) / 64;
-#pragma unroll
-      for (int j = 0; j < JR; ++j) {
-        const int task = slot + j * S;
-        const int ms = task / p.RS;
-        const int rl = task - ms * p.RS;
-        task_row[j] = rl;
-        code_off[j] = (ms * p.RS + rl) * rcb + uu * 16;
-        group_off[j] = (ms * p.RS + rl) * rgb + group_in_row * 2;
-      }
-
-      const OpRows o = op_rows(p);
-      for (int row = o.r0; row < o.r1;) {
-        const int n = min(p.RS, o.r1 - row);
-        if (!mbar_wait(smem_u32(&full_bar[ring.slot]), ring.phase, &g_status)) return;
-        if (active) {
-          const uint8_t* st = smem + static_cast<size_t>(ring.slot) * a.slot_bytes;
-          float acc[JR];
-#pragma unroll
-          for (int j = 0; j < JR; ++j) {
-            const __half sv = *reinterpret_cast<const __half*>(st + scales_off + group_off[j]);
-            const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
-            const float v = slice_dot<4>(st + code_off[j], xr, __half2float(sv), __half2float(bv),
-                                         xs_scaled);
-            acc[j] = task_row[j] < n ? v : 0.f;
-          }
-          float* rs = red + static_cast<size_t>(ring.slot) * a.red_slot_floats;
-          constexpr int kLanesPerRow = 32 / JR;
-          const float v = warp_reduce_rows<JR>(acc, lane);
-          if ((lane & (kLanesPerRow - 1)) == 0)
-            rs[(slot + (lane / kLanesPerRow) * S) * wpt + wit] = v;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&part_bar[ring.slot]));
-          mbar_arrive(smem_u32(&empty_bar[ring.slot]));
-        }
-        ring.advance();
-        row = next_row(o, row, n);
-      }
+      if (!consume_op<kSliceK, kStackJR>(a, l, k, t, lane, ring, smem, red, full_bar, part_bar,
+                                         empty_bar))
+        return;
     }
   }
 }
@@ -478,7 +510,7 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   a.eps = shape->eps;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  auto* kern = stack_kernel<kStackJR>;
+  auto* kern = stack_kernel;
   if (dev < 32 && !((g_attr_done.load(std::memory_order_acquire) >> dev) & 1u)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024) !=
         cudaSuccess)
