@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   const int group_in_row = (uu * KPT) / 64;
   // Task j of this thread in every stage: matrix slot and row, and the
   // shared-memory offsets of its slice.
-  int task_row[JR], code_off[JR], group_off[JR];
+  int code_off[JR], group_off[JR];
 #pragma unroll
   for (int j = 0; j < JR; ++j) {
     const int task = slot + j * S;
@@ -454,7 +454,6 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       ms = task / a.RS;
       rl = task - ms * a.RS;
     }
-    task_row[j] = rl;
     code_off[j] = (ms * a.RS + rl) * rcb + uu * TK::kCodeBytes;
     group_off[j] = (ms * a.RS + rl) * rgb + group_in_row * 2;
   }
@@ -464,8 +463,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     const int s = wk.slot;
     if (!mbar_wait(smem_u32(&full_bar[s]), wk.phase, &g_status)) return;
     const uint8_t* st = smem + static_cast<size_t>(s) * a.stage_bytes;
-    bool slot_ok = expert_ok;
-    if (MODE == kMoeUp) slot_ok = s_eidx[wk.expert_slot] >= 0;
+    const bool slot_ok = expert_ok;
 
     float acc[JR];
 #pragma unroll
@@ -474,7 +472,11 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
       const float v = task_dot<BITS, KPT>(st + codes_off + code_off[j], xp, __half2float(sv),
                                           __half2float(bv), xs_scaled);
-      acc[j] = (task_row[j] < n && slot_ok) ? v : 0.f;
+      // Tasks of rows past a partial stage's end read stale (valid) shared
+      // memory; their partials land in reduction slots the epilogue never
+      // reads, so no mask.  An invalid MoE expert's partial must be zero:
+      // its slot weight is zero, but its stale scale may not be finite.
+      acc[j] = (MODE == kMoeDown && !slot_ok) ? 0.f : v;
     }
 
     // Warp partials of this stage's tasks into the stage's slots.

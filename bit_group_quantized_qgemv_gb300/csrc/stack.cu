@@ -179,14 +179,13 @@ __device__ __forceinline__ bool consume_op(const StackArgs& a, int l, int k, int
       load_task_x<4, KPT>(op_input(a, l, k), gam, nullptr, k0, xp, xs_scaled);
     }
   }
-  int task_row[JR], code_off[JR], group_off[JR];
+  int code_off[JR], group_off[JR];
   const int group_in_row = (uu * KPT) / 64;
 #pragma unroll
   for (int j = 0; j < JR; ++j) {
     const int task = slot + j * S;
     const int ms = task / p.RS;
     const int rl = task - ms * p.RS;
-    task_row[j] = rl;
     code_off[j] = (ms * p.RS + rl) * rcb + uu * TK::kCodeBytes;
     group_off[j] = (ms * p.RS + rl) * rgb + group_in_row * 2;
   }
@@ -204,7 +203,7 @@ __device__ __forceinline__ bool consume_op(const StackArgs& a, int l, int k, int
         const __half bv = *reinterpret_cast<const __half*>(st + biases_off + group_off[j]);
         const float v = task_dot<4, KPT>(st + code_off[j], xp, __half2float(sv), __half2float(bv),
                                          xs_scaled);
-        acc[j] = task_row[j] < n ? v : 0.f;
+        acc[j] = v;  // rows past a partial stage's end: partials never read
       }
       float* rs = red + static_cast<size_t>(ring.slot) * a.red_slot_floats;
       constexpr int kLanesPerRow = 32 / JR;
