@@ -54,8 +54,10 @@ def parse_args():
                    help="skip the oracle CPU-baseline leg")
     p.add_argument("--no-unfused", action="store_true",
                    help="skip the single-op CUDA-graph comparison")
-    p.add_argument("--op", choices=["stack", "qkv", "o_proj", "swiglu", "down", "moe"],
-                   default="stack", help="time one fused op alone instead of the stack")
+    p.add_argument("--op", choices=["stack", "qkv", "o_proj", "swiglu", "down", "moe",
+                                    "lm_head"],
+                   default="stack", help="time one fused op alone instead of the stack "
+                                         "(lm_head: the Qwen3-0.6B-shaped 1024->151936 matvec)")
     return p.parse_args()
 
 
@@ -419,6 +421,13 @@ def run_op(args):
         gu, dn = synth.moe_experts(3, 0, 8)
         base = (up(gu), up(dn))
         nbytes = acc.moe_token_bytes()
+    elif args.op == "lm_head":
+        c = synth.QWEN06B
+        w = synth.quant_weight(synth.rng(2, 0, synth.TID["lm_head"]), c["vocab"], c["hidden"])
+        base = (up(w),)
+        nbytes = acc.matvec_bytes(c["vocab"], c["hidden"], 4)
+        x = torch.from_numpy(synth.activation(synth.rng(2, 0, synth.TID["x"]),
+                                              c["hidden"])).to(dev)
     elif args.op == "swiglu":
         base = (up(layer["gate"]), up(layer["up"]))
         nbytes = ops["gate_up_swiglu"]
@@ -430,7 +439,7 @@ def run_op(args):
     copies = max(2, int(3 * 129e6 // nbytes) + 1)
     ws = [tuple(tuple(t.clone() for t in w) for w in base) for _ in range(copies)]
     xi = torch.randn(I, device=dev).half()
-    y = torch.empty(max(I, 6144), device=dev).half()
+    y = torch.empty(max(I, 6144, synth.QWEN06B["vocab"]), device=dev).half()
     idx = torch.tensor([0, 3, 5, 6], dtype=torch.int32, device=dev)
     wt = torch.tensor([0.4, 0.3, 0.2, 0.1], dtype=torch.float32, device=dev)
     work = torch.empty(4 * 1024, dtype=torch.float32, device=dev)
@@ -445,6 +454,8 @@ def run_op(args):
             q.swiglu_qgemv(w[0], w[1], x, g2, eps, h=y[:I])
         elif args.op == "down":
             q.qgemv_w4g64(w[0], xi, y=y[:H], residual=x)
+        elif args.op == "lm_head":
+            q.qgemv_w4g64(w[0], x, y=y[:synth.QWEN06B["vocab"]])
         else:
             q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y[:H], workspace=work)
 
