@@ -54,10 +54,10 @@ def parse_args():
                    help="skip the oracle CPU-baseline leg")
     p.add_argument("--no-unfused", action="store_true",
                    help="skip the single-op CUDA-graph comparison")
-    p.add_argument("--op", choices=["stack", "qkv", "o_proj", "swiglu", "down", "moe",
-                                    "lm_head"],
-                   default="stack", help="time one fused op alone instead of the stack "
-                                         "(lm_head: the Qwen3-0.6B-shaped 1024->151936 matvec)")
+    p.add_argument("--op", default="stack",
+                   help="time one op or configuration unit alone instead of the stack: "
+                        "qkv, o_proj, swiglu, down, moe, lm_head, gemv1024, qwen_stack, "
+                        "w2_layer, m2, m4, m8, m8_w2, or all")
     return p.parse_args()
 
 
@@ -390,10 +390,21 @@ def run_own(args):
     return 0
 
 
+OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "gemv1024", "qwen_stack",
+       "w2_layer", "m2", "m4", "m8", "m8_w2"]
+
+
 def run_op(args):
-    """One fused op of the Llama-8B-shaped layer (or one MoE token), timed
-    alone: a CUDA graph of launches on rotating device copies (more bytes
-    than L2), replayed; one JSON line."""
+    """One op (or one workload configuration's unit of work) timed alone:
+    a CUDA graph of calls on rotating device copies (more bytes than L2),
+    replayed; one JSON line per op.  `--op all` runs every entry of OPS."""
+    names = OPS if args.op == "all" else [args.op]
+    for name in names:
+        run_one_op(args, name)
+    return 0
+
+
+def run_one_op(args, name):
     import numpy as np
     import torch
 
@@ -411,83 +422,184 @@ def run_op(args):
         return (torch.from_numpy(np.ascontiguousarray(w.codes).view(np.int32)).to(dev),
                 torch.from_numpy(w.scales).to(dev), torch.from_numpy(w.biases).to(dev))
 
-    layer = synth.llama_layer(1, 0, 4)
-    H, I = synth.LLAMA8B["hidden"], synth.LLAMA8B["inter"]
-    x = torch.from_numpy(layer["x"]).to(dev)
-    g1 = torch.from_numpy(layer["gamma1"]).to(dev)
-    g2 = torch.from_numpy(layer["gamma2"]).to(dev)
-    ops = dict(acc.llama8b_layer_ops(4))
-    if args.op == "moe":
+    c8, cq = synth.LLAMA8B, synth.QWEN06B
+    H, I = c8["hidden"], c8["inter"]
+    qkv_n = (c8["n_q"] + 2 * c8["n_kv"]) * c8["head_dim"]
+    graph = True
+    config = "config 1: Llama-3.1-8B-shaped layer op"
+    if name in ("qkv", "o_proj", "swiglu", "down"):
+        layer = synth.llama_layer(1, 0, 4)
+        x = torch.from_numpy(layer["x"]).to(dev)
+        ops = dict(acc.llama8b_layer_ops(4))
+        xi = torch.randn(I, device=dev).half()
+        g = torch.from_numpy(layer["gamma1" if name == "qkv" else "gamma2"]).to(dev)
+        y = torch.empty(max(I, qkv_n), device=dev).half()
+        if name == "swiglu":
+            base = (up(layer["gate"]), up(layer["up"]))
+            nbytes = ops["gate_up_swiglu"]
+        else:
+            key = {"qkv": "qkv", "o_proj": "o", "down": "down"}[name]
+            base = (up(layer[key]),)
+            nbytes = ops[{"qkv": "rmsnorm_qkv", "o_proj": "o_proj_residual",
+                          "down": "down_residual"}[name]]
+
+        def call(w):
+            if name == "qkv":
+                q.rmsnorm_qgemv(w[0], x, g, eps, y=y[:qkv_n])
+            elif name == "o_proj":
+                q.qgemv_w4g64(w[0], x, y=y[:H], residual=x)
+            elif name == "swiglu":
+                q.swiglu_qgemv(w[0], w[1], x, g, eps, h=y[:I])
+            else:
+                q.qgemv_w4g64(w[0], xi, y=y[:H], residual=x)
+        launches = 1
+    elif name == "moe":
+        config = "config 3: MoE token, 4 of 512 experts, combine + residual"
         gu, dn = synth.moe_experts(3, 0, 8)
         base = (up(gu), up(dn))
         nbytes = acc.moe_token_bytes()
-    elif args.op == "lm_head":
-        c = synth.QWEN06B
-        w = synth.quant_weight(synth.rng(2, 0, synth.TID["lm_head"]), c["vocab"], c["hidden"])
-        base = (up(w),)
-        nbytes = acc.matvec_bytes(c["vocab"], c["hidden"], 4)
-        x = torch.from_numpy(synth.activation(synth.rng(2, 0, synth.TID["x"]),
-                                              c["hidden"])).to(dev)
-    elif args.op == "swiglu":
-        base = (up(layer["gate"]), up(layer["up"]))
-        nbytes = ops["gate_up_swiglu"]
-    else:
-        key = {"qkv": "qkv", "o_proj": "o", "down": "down"}[args.op]
-        base = (up(layer[key]),)
-        nbytes = ops[{"qkv": "rmsnorm_qkv", "o_proj": "o_proj_residual",
-                      "down": "down_residual"}[args.op]]
-    copies = max(2, int(3 * 129e6 // nbytes) + 1)
-    ws = [tuple(tuple(t.clone() for t in w) for w in base) for _ in range(copies)]
-    xi = torch.randn(I, device=dev).half()
-    y = torch.empty(max(I, 6144, synth.QWEN06B["vocab"]), device=dev).half()
-    idx = torch.tensor([0, 3, 5, 6], dtype=torch.int32, device=dev)
-    wt = torch.tensor([0.4, 0.3, 0.2, 0.1], dtype=torch.float32, device=dev)
-    work = torch.empty(4 * 1024, dtype=torch.float32, device=dev)
+        x = torch.from_numpy(synth.activation(synth.rng(3, 0, synth.TID["x"]), H)).to(dev)
+        idx = torch.tensor([0, 3, 5, 6], dtype=torch.int32, device=dev)
+        wt = torch.tensor([0.4, 0.3, 0.2, 0.1], dtype=torch.float32, device=dev)
+        work = torch.empty(4 * 1024, dtype=torch.float32, device=dev)
+        y = torch.empty(H, device=dev).half()
 
-    def call(i):
-        w = ws[i % copies]
-        if args.op == "qkv":
-            q.rmsnorm_qgemv(w[0], x, g1, eps, y=y[:6144])
-        elif args.op == "o_proj":
-            q.qgemv_w4g64(w[0], x, y=y[:H], residual=x)
-        elif args.op == "swiglu":
-            q.swiglu_qgemv(w[0], w[1], x, g2, eps, h=y[:I])
-        elif args.op == "down":
-            q.qgemv_w4g64(w[0], xi, y=y[:H], residual=x)
-        elif args.op == "lm_head":
-            q.qgemv_w4g64(w[0], x, y=y[:synth.QWEN06B["vocab"]])
+        def call(w):
+            q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y, workspace=work)
+        launches = 2
+    elif name in ("lm_head", "gemv1024"):
+        if name == "lm_head":
+            config = "config 2: Qwen3-0.6B-shaped lm_head 1024->151936"
+            N, K, wl = cq["vocab"], cq["hidden"], 2
         else:
-            q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y[:H], workspace=work)
+            config = "config 0: single 4-bit g64 GEMV 1024x1024"
+            N, K, wl = 1024, 1024, 0
+        w0 = synth.quant_weight(synth.rng(wl, 0, synth.TID["lm_head" if wl == 2 else "qkv"]), N, K)
+        base = (up(w0),)
+        nbytes = acc.matvec_bytes(N, K, 4)
+        x = torch.from_numpy(synth.activation(synth.rng(wl, 0, synth.TID["x"]), K)).to(dev)
+        y = torch.empty(N, device=dev).half()
+
+        def call(w):
+            q.qgemv_w4g64(w[0], x, y=y)
+        launches = 1
+    elif name == "w2_layer":
+        config = "config 4: the five matvecs of one 8B-shaped layer at 2-bit"
+        layer = synth.llama_layer(4, 0, 2)
+        shapes = [("qkv", qkv_n, H), ("o", H, H), ("gate", I, H), ("up", I, H), ("down", H, I)]
+        base = tuple(up(layer[k]) for k, _, _ in shapes)
+        nbytes = sum(acc.matvec_bytes(n, k, 2) for _, n, k in shapes)
+        xs = {H: torch.randn(H, device=dev).half(), I: torch.randn(I, device=dev).half()}
+        y = torch.empty(max(I, qkv_n), device=dev).half()
+
+        def call(w):
+            for (key, n, k), wi in zip(shapes, w):
+                q.qgemv_w2g64(wi, xs[k], y=y[:n])
+        launches = len(shapes)
+    elif name in ("m2", "m4", "m8", "m8_w2"):
+        M = int(name[1])
+        bits = 2 if name.endswith("w2") else 4
+        config = "config 4: M=%d small batch, %d-bit, o_proj- and down-shaped" % (M, bits)
+        shapes = [(H, H), (H, I)]
+        base = tuple(up(synth.quant_weight(synth.rng(4, n + k, synth.TID["qkv"]), n, k, bits))
+                     for n, k in shapes)
+        nbytes = sum(acc.matvec_bytes(n, k, bits, M=M) for n, k in shapes)
+        xs = [torch.randn(M, k, device=dev).half() for _, k in shapes]
+        ys = [torch.empty(M, n, device=dev).half() for n, _ in shapes]
+        fn = q.qgemv_w2g64 if bits == 2 else q.qgemv_w4g64
+
+        def call(w):
+            for wi, xi_, yi in zip(w, xs, ys):
+                fn(wi, xi_, y=yi)
+        launches = 2
+    elif name == "qwen_stack":
+        config = "config 2: Qwen3-0.6B-shaped decode stack, 28 layers + lm_head"
+        graph = False  # one cooperative launch (+ lm_head) per token
+        nl = cq["layers"]
+        r = lambda t: synth.rng(2, 0, synth.TID[t])  # noqa: E731
+        Hq, Iq = cq["hidden"], cq["inter"]
+        Dq = cq["n_q"] * cq["head_dim"]
+        qn = (cq["n_q"] + 2 * cq["n_kv"]) * cq["head_dim"]
+        one = {"qkv": up(synth.quant_weight(r("qkv"), qn, Hq)),
+               "o": up(synth.quant_weight(r("o"), Hq, Dq)),
+               "gate": up(synth.quant_weight(r("gate"), Iq, Hq)),
+               "up": up(synth.quant_weight(r("up"), Iq, Hq)),
+               "down": up(synth.quant_weight(r("down"), Hq, Iq)),
+               "attn_norm": torch.from_numpy(synth.norm_gamma(r("gamma1"), Hq)).to(dev),
+               "mlp_norm": torch.from_numpy(synth.norm_gamma(r("gamma2"), Hq)).to(dev)}
+        layers = [{k: (tuple(t.clone() for t in v) if isinstance(v, tuple) else v.clone())
+                   for k, v in one.items()} for _ in range(nl)]
+        lm = up(synth.quant_weight(r("lm_head"), cq["vocab"], Hq))
+        shape = q.stack_shape(Hq, cq["n_q"], cq["n_kv"], cq["head_dim"], Iq, nl, eps)
+        descs = q.stack_layers(layers)
+        work = torch.empty(q.decode_stack_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+        x = torch.from_numpy(synth.activation(r("x"), Hq)).to(dev)
+        hidden = torch.empty(Hq, device=dev).half()
+        logits = torch.empty(cq["vocab"], device=dev).half()
+        layer_bytes = (acc.matvec_bytes(qn, Hq, 4, gamma=True) +
+                       acc.matvec_bytes(Hq, Dq, 4, residual=True) +
+                       acc.weight_bytes(2 * Iq, Hq, 4) + 2 * Hq + 2 * Hq + 2 * Iq +
+                       acc.matvec_bytes(Hq, Iq, 4, residual=True))
+        nbytes = nl * layer_bytes + acc.matvec_bytes(cq["vocab"], Hq, 4)
+        base = (lm,)
+
+        def call(w):
+            q.decode_stack(descs, shape, x, y=hidden, workspace=work)
+            q.qgemv_w4g64(w[0], hidden, y=logits)
+        launches = 2
+    else:
+        raise SystemExit("unknown op " + name)
+
+    weight_bytes = sum(t.numel() * t.element_size() for wt in base for t in wt)
+    copies = 1 if name == "qwen_stack" else max(2, int(3 * 129e6 // max(weight_bytes, 1)) + 1)
+    if name == "gemv1024":
+        copies = max(copies, 512)
+    ws = [base] + [tuple(tuple(t.clone() for t in wt) for wt in base) for _ in range(copies - 1)]
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
         for i in range(copies):
-            call(i)
+            call(ws[i])
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(copies):
-            call(i)
-    reps = max(1, args.steps // copies)
-    for _ in range(max(3, args.warmup // copies)):
-        graph.replay()
-    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        graph.replay()
-    e1.record()
+    if graph:
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            for i in range(copies):
+                call(ws[i])
+        reps = max(1, args.steps // copies)
+        for _ in range(max(3, args.warmup // copies)):
+            cg.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            cg.replay()
+        e1.record()
+        n_calls = reps * copies
+    else:
+        reps = max(1, min(args.steps, 300))
+        for i in range(max(3, min(args.warmup, 20))):
+            call(ws[0])
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(reps):
+            call(ws[0])
+        e1.record()
+        n_calls = reps
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (reps * copies)
+    ms = e0.elapsed_time(e1) / n_calls
     peak, peak_kind = measured_peak()
-    print(json.dumps({"op": args.op, "metric": "achieved HBM GB/s of one op (CUDA-graph replays)",
-                      "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                      "us_per_launch": round(ms * 1e3, 3), "bytes_per_launch": nbytes,
-                      "weight_copies": copies, "launches_timed": reps * copies, "peak": peak,
-                      "peak_kind": peak_kind, "device_status": q.device_status()}), flush=True)
-    return 0
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"op": name, "config": config,
+                      "metric": "achieved HBM GB/s of one unit (CUDA-graph replays)" if graph
+                      else "achieved HBM GB/s of one unit (stream launches)",
+                      "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 3),
+                      "bytes_per_call": nbytes, "launches_per_call": launches,
+                      "weight_copies": copies, "calls_timed": n_calls, "peak": peak,
+                      "peak_kind": peak_kind, "frac": round(gbs / peak, 4),
+                      "device_status": q.device_status()}), flush=True)
 
 
 # ------------------------------------------------------- CPU baseline

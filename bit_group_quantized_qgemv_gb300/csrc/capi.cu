@@ -71,10 +71,31 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
   a.K = K;
   a.M = M;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms);
-  if (M == 1 && p.ok && aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
-      aligned(x, 16))
-    return finish(qgemv::stream_plain(bits, p, a, st, dev));
+  const bool al16 = aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
+                    aligned(x, 16);
+  if (M == 1) {
+    const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms);
+    if (p.ok && al16) return finish(qgemv::stream_plain(bits, p, a, st, dev));
+    return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
+  }
+  // Small batch: one pass holding all M rows when it fits, else passes of
+  // at most 4 rows (each pass streams the weights once).
+  const StreamPlan p = qgemv::make_batch_plan(bits, K, N, M, sms);
+  if (al16 && p.ok) return finish(qgemv::stream_batch(bits, p, a, st, dev));
+  const StreamPlan p4 = qgemv::make_batch_plan(bits, K, N, 4, sms);
+  if (al16 && p4.ok) {
+    for (int m0 = 0; m0 < M; m0 += 4) {
+      StreamArgs ap = a;
+      ap.M = M - m0 < 4 ? M - m0 : 4;
+      const StreamPlan pp = qgemv::make_batch_plan(bits, K, N, ap.M < 2 ? 2 : ap.M, sms);
+      ap.x = a.x + static_cast<size_t>(m0) * K;
+      ap.y = a.y + static_cast<size_t>(m0) * N;
+      if (a.residual) ap.residual = a.residual + static_cast<size_t>(m0) * N;
+      const cudaError_t e = qgemv::stream_batch(bits, pp, ap, st, dev);
+      if (e != cudaSuccess) return finish(e);
+    }
+    return QGEMV_OK;
+  }
   return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
 }
 
@@ -273,7 +294,7 @@ int qgemv_device_status(unsigned* flags) {
   unsigned v = 0;
   if (qgemv::status_plain(&v) != cudaSuccess || qgemv::status_norm_swiglu(&v) != cudaSuccess ||
       qgemv::status_moe(&v) != cudaSuccess || qgemv::status_generic(&v) != cudaSuccess ||
-      qgemv::status_stack(&v) != cudaSuccess)
+      qgemv::status_stack(&v) != cudaSuccess || qgemv::status_batch(&v) != cudaSuccess)
     return QGEMV_EDEVICE;
   *flags = v;
   return QGEMV_OK;

@@ -51,6 +51,7 @@ struct StreamArgs {
 struct StreamPlan {
   bool ok = false;
   int kpt = 0;  // k per thread and task (32: half a quantisation group)
+  int mb = 1;   // batch rows a consumer thread holds (small-batch kernel)
   int ub = 0, tg = 0, t = 0, s = 0, jr = 0, rs = 0, ns = 0, stage_bytes = 0, grid = 0;
   int red_bytes = 0;   // partial-sum slots per stage
   int interleave = 0;  // 1: CTAs take stages round-robin
@@ -123,6 +124,56 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   return p;
 }
 
+// Plan of the small-batch kernel for M = 2..8 activation rows: a thread
+// holds its k of all MB >= M rows in registers, so MB * KPT is bounded
+// (MB = 2: KPT = 32, K <= 16384; MB = 4: KPT = 32, K <= 14336; MB = 8:
+// KPT = 16 with at most 256 consumer threads, i.e. K <= 4096).  ok = false
+// when it does not apply.
+inline StreamPlan make_batch_plan(int bits, int K, long long rows, int M, int sms,
+                                  int stage_limit = 40 * 1024, int ring_budget = 200 * 1024) {
+  StreamPlan p;
+  if ((bits != 4 && bits != 2) || M < 2 || M > kMaxM || rows <= 0 || sms <= 0) return p;
+  const int mb = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
+  const int kpt = (mb == 8) ? 16 : 32;
+  if (K % (32 * kpt) != 0) return p;
+  const int tg = K / kpt;
+  const int target = (mb == 2) ? 512 : 256;
+  if (tg > (mb == 8 ? 256 : (mb == 4 ? 448 : 512))) return p;  // the kernels' launch bounds
+  int s = target / tg;
+  if (s < 1) s = 1;
+  const int t = s * tg;
+  int jr = (mb == 2) ? 4 : 2;
+  const int task_bytes = K * bits / 8 + 2 * (K / 32);
+  while (jr > 1 && static_cast<long long>(s) * jr * task_bytes > stage_limit) jr /= 2;
+  const int rs = s * jr;
+  const long long stage = static_cast<long long>(rs) * task_bytes;
+  if (stage > 100 * 1024) return p;
+  const int red = ((rs * mb * (tg / 32) + 3) & ~3) * static_cast<int>(sizeof(float));
+  int ns = static_cast<int>(ring_budget / (stage + red));
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) return p;
+  p.ok = true;
+  p.kpt = kpt;
+  p.mb = mb;
+  p.ub = kpt * bits / 8;
+  p.tg = tg;
+  p.t = t;
+  p.s = s;
+  p.jr = jr;
+  p.rs = rs;
+  p.ns = ns;
+  p.stage_bytes = static_cast<int>(stage);
+  p.red_bytes = red;
+  p.smem_bytes = ns * (static_cast<int>(stage) + red);
+  p.grid = static_cast<int>(rows < sms ? rows : sms);
+  const long long stages = (rows + rs - 1) / rs;
+  if (stages >= 4LL * sms) {
+    p.interleave = 1;
+    p.grid = sms;
+  }
+  return p;
+}
+
 // Entry points of the kernel translation units (each returns the CUDA
 // error of its launch).
 cudaError_t stream_plain(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
@@ -132,6 +183,8 @@ cudaError_t stream_swiglu(const StreamPlan& p, const StreamArgs& a, cudaStream_t
 cudaError_t stream_moe_up(const StreamPlan& p, const StreamArgs& a, cudaStream_t st, int device);
 cudaError_t stream_moe_down(const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                             int device);
+cudaError_t stream_batch(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
+                         int device);
 cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t st);
 cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n_kv,
                                   int head_dim, cudaStream_t st);
@@ -142,5 +195,6 @@ cudaError_t status_norm_swiglu(unsigned* out);
 cudaError_t status_moe(unsigned* out);
 cudaError_t status_generic(unsigned* out);
 cudaError_t status_stack(unsigned* out);
+cudaError_t status_batch(unsigned* out);
 
 }  // namespace qgemv
