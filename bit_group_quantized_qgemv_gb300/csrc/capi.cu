@@ -294,7 +294,7 @@ int qgemv_device_status(unsigned* flags) {
   unsigned v = 0;
   if (qgemv::status_plain(&v) != cudaSuccess || qgemv::status_norm_swiglu(&v) != cudaSuccess ||
       qgemv::status_moe(&v) != cudaSuccess || qgemv::status_generic(&v) != cudaSuccess ||
-      qgemv::status_stack(&v) != cudaSuccess || qgemv::status_batch(&v) != cudaSuccess)
+      qgemv::status_batch(&v) != cudaSuccess)
     return QGEMV_EDEVICE;
   *flags = v;
   return QGEMV_OK;

@@ -193,6 +193,8 @@ cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t
 
 __global__ void attention_seq1_kernel(const __half* __restrict__ qkv, __half* __restrict__ out,
                                       int n_q, int n_kv, int head_dim) {
+  pdl_launch_dependents();
+  pdl_wait();  // qkv comes from the previous kernel
   const long long total = static_cast<long long>(n_q) * head_dim;
   const int group = n_q / n_kv;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -209,9 +211,16 @@ cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n
   long long blocks = (total + 255) / 256;
   if (blocks > 1024) blocks = 1024;
   if (blocks < 1) blocks = 1;
-  attention_seq1_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(qkv, out, n_q, n_kv,
-                                                                        head_dim);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_seq1_kernel, qkv, out, n_q, n_kv, head_dim);
 }
 
 cudaError_t status_generic(unsigned* out) {

@@ -46,6 +46,10 @@ struct StreamArgs {
   int TG, S, RS, NS;        // launch plan of the streaming kernel
   int stage_bytes;
   int interleave;           // 1: CTAs take stages round-robin (see StageWalker)
+  // kPlain: when gather_hd > 0, x is the attention output of a decode over
+  // one cached position gathered from qkv (x points at qkv): query head h
+  // reads value head h / (gather_nq / gather_nkv) of head_dim gather_hd.
+  int gather_nq, gather_nkv, gather_hd;
 };
 
 struct StreamPlan {
@@ -194,7 +198,6 @@ cudaError_t status_plain(unsigned* out);
 cudaError_t status_norm_swiglu(unsigned* out);
 cudaError_t status_moe(unsigned* out);
 cudaError_t status_generic(unsigned* out);
-cudaError_t status_stack(unsigned* out);
 cudaError_t status_batch(unsigned* out);
 
 }  // namespace qgemv

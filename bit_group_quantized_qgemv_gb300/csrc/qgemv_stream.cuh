@@ -292,6 +292,10 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   const int scales_off = MS * a.RS * rcb;
   const int biases_off = scales_off + MS * a.RS * rgb;
 
+  // The next kernel of the stream may start launching now: its producer
+  // streams weights (which no kernel writes) while its consumers wait for
+  // this grid (pdl_wait below).
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -300,6 +304,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     }
     fence_mbar_init();
     if (MODE == kMoeUp || MODE == kMoeDown) {
+      pdl_wait();  // the expert indices and weights may come from the previous kernel
       for (int k = 0; k < a.top_k; ++k) {
         const int e = a.idx[k];
         const bool ok = e >= 0 && e < a.n_experts;
@@ -380,7 +385,9 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
 
   if (epi) {
     // Epilogue warp: RMS of the input (RMSNorm modes), then finish every
-    // stage's rows once all partials are in.
+    // stage's rows once all partials are in.  It reads x and residuals and
+    // writes y, so it waits for the previous kernel first.
+    pdl_wait();
     const float rstd = use_gamma ? warp_rstd(a.x, a.K, a.eps, lane) : 1.f;
     for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
       const int n = wk.rows();
@@ -433,11 +440,22 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   // block-wide staging or barrier, so each warp starts on its own.
   uint32_t xp[TK::kXRegs];
   float xs_scaled;
+  pdl_wait();  // x may come from the previous kernel
   if (MODE == kMoeDown)
     load_task_x<BITS, KPT>(nullptr, nullptr, a.xf + static_cast<size_t>(ek) * a.K, uu * KPT, xp,
                            xs_scaled);
-  else
+  else if (MODE == kPlain && a.gather_hd > 0) {
+    // a KPT-k slice lies inside one head (head_dim % KPT == 0, host-checked)
+    const int k0 = uu * KPT;
+    const int head = k0 / a.gather_hd;
+    const __half* src =
+        a.x + static_cast<long long>(a.gather_nq + a.gather_nkv + head / (a.gather_nq / a.gather_nkv)) *
+                  a.gather_hd +
+        (k0 - head * a.gather_hd);
+    load_task_x<BITS, KPT>(src, nullptr, nullptr, 0, xp, xs_scaled);
+  } else {
     load_task_x<BITS, KPT>(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * KPT, xp, xs_scaled);
+  }
   const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
   const int group_in_row = (uu * KPT) / 64;
   // Task j of this thread in every stage: matrix slot and row, and the
@@ -495,6 +513,25 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   }
 }
 
+// Launch with programmatic stream serialisation allowed, so the kernel may
+// start while the previous kernel of the stream finishes (see
+// pdl_launch_dependents / pdl_wait).
+template <typename F>
+inline cudaError_t launch_pdl(F* kernel, const StreamPlan& p, const StreamArgs& a,
+                              cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(p.t + 64));
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 // Set the dynamic shared-memory limit once per (kernel, device).
 template <typename F>
 inline cudaError_t ensure_smem_attr(F* kernel, int bytes, unsigned* done_mask, int device) {
@@ -519,8 +556,7 @@ inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
   a.interleave = p.interleave;
-  k<<<p.grid, p.t + 64, p.smem_bytes, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, p, a, stream);
 }
 
 // Dispatch on the plan's tasks per thread.

@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
   const int scales_off = a.RS * rcb;
   const int biases_off = scales_off + a.RS * rgb;
 
+  pdl_launch_dependents();  // see stream_kernel
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
 
   // ------------------------------------------------------------ epilogue
   if (epi) {
+    pdl_wait();  // residuals and y belong to the stream order
     for (StageWalker wk(r0, r1, a.RS, NS, 0, stride); wk.more();) {
       const int n = wk.rows();
       const int s = wk.slot;
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
   // ----------------------------------------------------------- consumers
   uint32_t xp[MB][KPT / 2];
   float xs[MB];
+  pdl_wait();  // x may come from the previous kernel
 #pragma unroll
   for (int m = 0; m < MB; ++m) {
     if (m < M) {
@@ -335,8 +338,7 @@ cudaError_t launch_batch_t(const StreamPlan& p, StreamArgs a, cudaStream_t strea
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
   a.interleave = p.interleave;
-  k<<<p.grid, p.t + 64, p.smem_bytes, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, p, a, stream);
 }
 
 template <int BITS>

@@ -227,7 +227,7 @@ typedef struct {
   float eps;
 } qgemv_stack_shape;
 
-/* Workspace bytes qgemv_decode_stack needs (counters, qkv, h, act, x). */
+/* Workspace bytes qgemv_decode_stack needs (qkv, h, act, x ping-pong). */
 size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape *shape);
 
 /*
@@ -235,10 +235,12 @@ size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape *shape);
  * descriptors of device pointers (all 16-byte aligned); x, y [hidden] fp16
  * device (16-byte aligned, may not overlap the workspace); workspace:
  * device, 256-byte aligned, >= qgemv_decode_stack_workspace_bytes bytes,
- * contents on entry ignored.  Checks: 1 <= n_layers <= 64, n_q % n_kv == 0,
+ * contents on entry ignored.  Checks: n_layers >= 1, n_q % n_kv == 0,
  * head_dim % 32 == 0, hidden, n_q*head_dim and inter multiples of 1024 and at
- * most 16384, eps > 0.  Enqueues a memset of the workspace's counters and
- * one cooperative launch on `stream`.
+ * most 16384, eps > 0.  Enqueues 4 * n_layers streaming-kernel launches on
+ * `stream` (programmatic dependent launch between them: each op's weights
+ * start streaming while the previous op finishes); calls that share a
+ * workspace must not overlap on the GPU.
  */
 int qgemv_decode_stack(const qgemv_stack_layer *layers, const qgemv_stack_shape *shape,
                        const uint16_t *x, uint16_t *y, void *workspace, size_t workspace_bytes,
