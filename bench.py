@@ -543,10 +543,11 @@ def run_one_op(args, name):
         def call(w):
             for wi, xi_, yi in zip(w, xs, ys):
                 fn(wi, xi_, y=yi)
-        launches = 2
+        # M = 8 holds 16 k per thread, so K = 14336 runs as two 4-row passes
+        launches = 3 if M == 8 else 2
     elif name == "qwen_stack":
         config = "config 2: Qwen3-0.6B-shaped decode stack, 28 layers + lm_head"
-        graph = False  # one cooperative launch (+ lm_head) per token
+        graph = False  # one qgemv_decode_stack call (+ lm_head) per token
         nl = cq["layers"]
         r = lambda t: synth.rng(2, 0, synth.TID[t])  # noqa: E731
         Hq, Iq = cq["hidden"], cq["inter"]
@@ -578,7 +579,7 @@ def run_one_op(args, name):
         def call(w):
             q.decode_stack(descs, shape, x, y=hidden, workspace=work)
             q.qgemv_w4g64(w[0], hidden, y=logits)
-        launches = 2
+        launches = 4 * nl + 1
     else:
         raise SystemExit("unknown op " + name)
 
