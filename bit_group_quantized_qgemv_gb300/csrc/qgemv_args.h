@@ -68,7 +68,7 @@ struct StreamPlan {
 // that a row's TG = K/KPT tasks span whole warps and every scale row is a
 // multiple of 16 bytes.
 inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, int top_k,
-                                   int sms, int target_threads = 512, int max_jr = 4,
+                                   int sms, int target_threads = 256, int max_jr = 8,
                                    int stage_limit = 40 * 1024, int ring_budget = 200 * 1024,
                                    bool interleave_ok = true) {
   StreamPlan p;
