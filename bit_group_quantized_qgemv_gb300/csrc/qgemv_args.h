@@ -94,6 +94,14 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   while (jr > 1 && (static_cast<long long>(s) * jr * task_bytes > stage_limit || (s * jr) % ms))
     jr /= 2;
   if ((s * jr) % ms) return p;
+  // An op of at most one stage per CTA: the smallest stage that still holds
+  // a CTA's rows (the tasks of rows past a CTA's end are computed and
+  // discarded, so a mostly empty stage costs compute for nothing).
+  if (mode == kPlain || mode == kNorm || mode == kSwiglu) {
+    const long long rpc = (rows + sms - 1) / sms;
+    while (jr > 1 && (s * (jr / 2)) % ms == 0 && static_cast<long long>(s) * (jr / 2) / ms >= rpc)
+      jr /= 2;
+  }
   const int tasks = s * jr;
   const int rs = tasks / ms;
   const long long stage = static_cast<long long>(tasks) * task_bytes;
