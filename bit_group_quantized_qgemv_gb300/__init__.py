@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     qgemv_w2g64,
     qgemv_w4g64,
     rmsnorm_qgemv,
+    selftest_wait_timeout,
     strerror,
     swiglu_qgemv,
     version,

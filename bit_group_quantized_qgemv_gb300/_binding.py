@@ -37,6 +37,7 @@ _SIGS = {
     "qgemv_last_cuda_error": (_I, []),
     "qgemv_device_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_version": (_I, []),
+    "qgemv_selftest_wait_timeout": (_I, [ctypes.c_uint, ctypes.c_void_p]),
 }
 
 #: Names the C header declares (the binding exposes each one).
@@ -289,6 +290,14 @@ def device_status() -> int:
     flags = ctypes.c_uint(0)
     _check(lib.qgemv_device_status(ctypes.byref(flags)), "qgemv_device_status")
     return int(flags.value)
+
+
+def selftest_wait_timeout(limit_us: int = 2000, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (qgemv_selftest_wait_timeout): a
+    wait that nothing satisfies gives up after limit_us and sets bit 0 of
+    the device status word."""
+    _check(lib.qgemv_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "qgemv_selftest_wait_timeout")
 
 
 def last_cuda_error() -> int:

@@ -300,6 +300,14 @@ int qgemv_device_status(unsigned* flags) {
   return QGEMV_OK;
 }
 
+int qgemv_selftest_wait_timeout(unsigned limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return QGEMV_EINVAL;
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  return finish(qgemv::selftest_wait_launch(static_cast<uint64_t>(limit_us) * 1000ull,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int qgemv_version(void) { return 100; }
 
 }  // extern "C"

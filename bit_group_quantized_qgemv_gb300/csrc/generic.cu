@@ -223,6 +223,23 @@ cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n
   return cudaLaunchKernelEx(&cfg, attention_seq1_kernel, qkv, out, n_q, n_kv, head_dim);
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that no
+// thread ever arrives on, with the given limit; the wait must give up, set
+// the timeout bit and return, leaving the context usable.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    (void)mbar_wait_for(smem_u32(&bar), 0, &g_status_generic, limit_ns);
+  }
+}
+
+cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t status_generic(unsigned* out) {
   unsigned v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_status_generic, sizeof(v));

@@ -198,6 +198,7 @@ cudaError_t stream_moe_down(const StreamPlan& p, const StreamArgs& a, cudaStream
 cudaError_t stream_batch(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                          int device);
 cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t st);
+cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t st);
 cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n_kv,
                                   int head_dim, cudaStream_t st);
 

@@ -66,16 +66,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // after about one second of wall time (the only legitimate waits are for
 // DRAM copies and sibling warps, microseconds at most), records the timeout
 // in *status and returns false: kernels then stop instead of hanging.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned* status,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (global_timer_ns() - t0 > 1000000000ull) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusWaitTimeout);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+  return mbar_wait_for(bar, parity, status, 1000000000ull);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {

@@ -260,6 +260,18 @@ int qgemv_last_cuda_error(void);
  */
 int qgemv_device_status(unsigned *flags);
 
+/*
+ * qgemv_selftest_wait_timeout -- health check of the bounded device waits
+ * every kernel uses: enqueues one tiny kernel on `stream` whose thread waits
+ * on a shared-memory mbarrier that nothing ever arrives on, with a limit of
+ * limit_us microseconds (1 .. 1000000) instead of the kernels' 1 s.  The
+ * wait gives up, sets bit 0 of the status word read by qgemv_device_status
+ * and the kernel returns: no trap, the context stays usable.  Returns
+ * QGEMV_OK, QGEMV_EINVAL (limit out of range), QGEMV_EDEVICE or
+ * QGEMV_ELAUNCH.
+ */
+int qgemv_selftest_wait_timeout(unsigned limit_us, void *stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int qgemv_version(void);
 

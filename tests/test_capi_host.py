@@ -29,7 +29,8 @@ def test_header_lists_the_boundary():
     names = header_functions()
     for n in ["qgemv_w4g64", "qgemv_w2g64", "rmsnorm_qgemv", "swiglu_qgemv",
               "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
-              "decode_attention_seq1", "qgemv_device_status"]:
+              "decode_attention_seq1", "qgemv_device_status",
+              "qgemv_selftest_wait_timeout", "qgemv_decode_stack"]:
         assert n in names
 
 
@@ -76,6 +77,8 @@ def test_bad_scalar_status(q):
     assert q.lib.moe_qgemv_combine(p, p, p, p, p, p, 0, 64, 64, p, p, 4, p, None, p, p,
                                    None, None) == -1
     assert q.lib.decode_attention_seq1(p, p, 6, 4, 128, None) == -1
+    for limit in (0, 1000001):
+        assert q.lib.qgemv_selftest_wait_timeout(limit, None) == -1
 
 
 def test_misaligned_status(q):
