@@ -46,6 +46,7 @@ struct StreamArgs {
   int TG, S, RS, NS;        // launch plan of the streaming kernel
   int stage_bytes;
   int interleave;           // 1: CTAs take stages round-robin (see StageWalker)
+  int prefill;              // stages the producer issues before the activations are in
   // kPlain: when gather_hd > 0, x is the attention output of a decode over
   // one cached position gathered from qkv (x points at qkv): query head h
   // reads value head h / (gather_nq / gather_nkv) of head_dim gather_hd.
@@ -60,7 +61,24 @@ struct StreamPlan {
   int red_bytes = 0;   // partial-sum slots per stage
   int interleave = 0;  // 1: CTAs take stages round-robin
   int smem_bytes = 0;  // dynamic shared memory: ns * (stage_bytes + red_bytes)
+  int prefill = 0;     // stages issued before every consumer warp has its activations
 };
+
+// Weight bytes a CTA's producer may have in flight before its consumers
+// have loaded their activations.  A kernel starts (programmatic dependent
+// launch) while its predecessor finishes; the activation loads, issued once
+// the predecessor's output is visible, queue behind whatever weight copies
+// are already outstanding, so issuing the whole ring at once delays them.
+// About 100 KB per SM keeps HBM busy meanwhile: measured on GB300 (32-layer
+// 8B stack) 1128 us with no limit, 1091 us with two 37 KB stages, 1078 us
+// with two (QKV, gate.up) or three (down: 32 KB) stages.
+constexpr int kPrefillBytes = 100 * 1024;
+
+inline int prefill_stages(int stage_bytes, int ns) {
+  int b = stage_bytes > 0 ? kPrefillBytes / stage_bytes : 1;
+  if (b < 1) b = 1;
+  return b < ns ? b : ns;
+}
 
 // Choose the thread counts, tasks per thread, rows per stage and ring depth
 // of the streaming kernel.  ok = false when it does not apply (the generic
@@ -124,6 +142,7 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
   p.stage_bytes = static_cast<int>(stage);
   p.red_bytes = red;
   p.smem_bytes = ns * (static_cast<int>(stage) + red);
+  p.prefill = prefill_stages(p.stage_bytes, ns);
   p.grid = static_cast<int>(rows < sms ? rows : sms);
   // Interleave stages across CTAs when that keeps the SMs within one stage
   // of each other (and, for kMoeUp, stages never straddle experts).
@@ -177,6 +196,7 @@ inline StreamPlan make_batch_plan(int bits, int K, long long rows, int M, int sm
   p.stage_bytes = static_cast<int>(stage);
   p.red_bytes = red;
   p.smem_bytes = ns * (static_cast<int>(stage) + red);
+  p.prefill = prefill_stages(p.stage_bytes, ns);
   p.grid = static_cast<int>(rows < sms ? rows : sms);
   const long long stages = (rows + rs - 1) / rs;
   if (stages >= 4LL * sms) {

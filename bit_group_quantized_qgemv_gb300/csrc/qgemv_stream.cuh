@@ -39,6 +39,10 @@
 //  * Every thread loads its own 32-k activation slice straight from global
 //    memory (L2): no block-wide staging, so no barrier among the consumer
 //    warps at all, and each starts as soon as its slice and stage are in.
+//    The producer issues only the plan's first `prefill` stages (about 100
+//    KB) before every consumer warp has its slice (the `xready` mbarrier):
+//    activation loads issued behind a full ring of outstanding weight copies
+//    waited about a microsecond longer.
 //  * Every mbarrier wait is bounded (about 1 s); a timeout sets a status bit
 //    and the waiting thread returns instead of hanging (no named barrier
 //    exists, so nothing is left waiting).
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t part_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t xready_bar;  // every consumer warp has its activations
   __shared__ int s_eidx[kMaxTopK];
   __shared__ float s_ewt[kMaxTopK];
 
@@ -302,6 +307,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       mbar_init(smem_u32(&part_bar[s]), static_cast<uint32_t>(T / 32));
       mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32 + 1));
     }
+    mbar_init(smem_u32(&xready_bar), static_cast<uint32_t>(T / 32));
     fence_mbar_init();
     if (MODE == kMoeUp || MODE == kMoeDown) {
       pdl_wait();  // the expert indices and weights may come from the previous kernel
@@ -324,6 +330,10 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
         const int n = wk.rows();
         const int s = wk.slot;
+        // After the first a.prefill stages, wait until the consumers hold
+        // their activations: their loads would otherwise queue behind the
+        // weight copies in flight.
+        if (issued == a.prefill && !mbar_wait(smem_u32(&xready_bar), 0, &g_status)) break;
         if (!mbar_wait(smem_u32(&empty_bar[s]), wk.phase ^ 1u, &g_status)) break;
         const uint32_t fb = smem_u32(&full_bar[s]);
         const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * a.stage_bytes);
@@ -456,6 +466,8 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   } else {
     load_task_x<BITS, KPT>(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * KPT, xp, xs_scaled);
   }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&xready_bar));
   const bool expert_ok = (MODE == kMoeDown) ? (s_eidx[ek] >= 0) : true;
   const int group_in_row = (uu * KPT) / 64;
   // Task j of this thread in every stage: matrix slot and row, and the
@@ -556,6 +568,7 @@ inline cudaError_t launch_stream_t(const StreamPlan& p, StreamArgs a, cudaStream
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
   a.interleave = p.interleave;
+  a.prefill = p.prefill;
   return launch_pdl(k, p, a, stream);
 }
 

@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t part_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t xready_bar;  // see stream_kernel
 
   const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
       mbar_init(smem_u32(&part_bar[s]), static_cast<uint32_t>(T / 32));
       mbar_init(smem_u32(&empty_bar[s]), static_cast<uint32_t>(T / 32 + 1));
     }
+    mbar_init(smem_u32(&xready_bar), static_cast<uint32_t>(T / 32));
     fence_mbar_init();
   }
   __syncthreads();
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
       for (StageWalker wk(r0, r1, a.RS, NS, 0, stride); wk.more();) {
         const int n = wk.rows();
         const int s = wk.slot;
+        if (issued == a.prefill && !mbar_wait(smem_u32(&xready_bar), 0, &g_status)) break;
         if (!mbar_wait(smem_u32(&empty_bar[s]), wk.phase ^ 1u, &g_status)) break;
         const uint32_t fb = smem_u32(&full_bar[s]);
         const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * a.stage_bytes);
@@ -283,6 +286,8 @@ __global__ void __launch_bounds__(MB == 8 ? 320 : (MB == 4 ? 512 : 576), 1)
       xs[m] = 0.f;
     }
   }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&xready_bar));
   const int group_in_row = (uu * KPT) / 64;
   int code_off[JR], group_off[JR];
 #pragma unroll
@@ -338,6 +343,7 @@ cudaError_t launch_batch_t(const StreamPlan& p, StreamArgs a, cudaStream_t strea
   a.NS = p.ns;
   a.stage_bytes = p.stage_bytes;
   a.interleave = p.interleave;
+  a.prefill = p.prefill;
   return launch_pdl(k, p, a, stream);
 }
 
