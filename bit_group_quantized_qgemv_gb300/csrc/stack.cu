@@ -19,8 +19,13 @@
 // cooperative persistent kernel synchronising its CTAs through completion
 // counters in global memory (1254 us against 1370 us per 32-layer token):
 // the hardware's grid dependency resolves sooner than a fence, an atomic and
-// a polled counter.
+// a polled counter.  The launches themselves go through a CUDA-graph cache
+// (below): eager launches cost more host time than the GPU needs for them.
 #include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
 
 #include "qgemv.h"
 #include "qgemv_args.h"
@@ -30,6 +35,85 @@ namespace {
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 size_t up256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// The 4 * n_layers launches of one call.  Arguments already validated.
+int enqueue_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape* shape,
+                  const uint16_t* x, uint16_t* y, void* workspace, int dev, int sms,
+                  cudaStream_t st);
+
+// CUDA-graph cache of the decode stack.  A call enqueues 4 * n_layers
+// kernels; on the Grace host of a GB300 node a cudaLaunchKernelEx costs about
+// 8 us of host time, close to an op's device time, so eager launches bound a
+// 32-layer token by the host (~1050 us).  Each distinct argument set (device,
+// shape, every pointer) is therefore captured once into a graph whose
+// instance later calls replay with one cudaGraphLaunch (~2 us of host time).
+// The kernels and their programmatic dependencies are the same either way.
+constexpr int kGraphCacheSize = 4;
+
+struct GraphEntry {
+  std::vector<uintptr_t> key;
+  cudaGraphExec_t exec = nullptr;
+  unsigned long long last_use = 0;
+};
+
+std::mutex g_graph_mu;
+GraphEntry g_graphs[kGraphCacheSize];
+unsigned long long g_graph_clock = 0;
+cudaStream_t g_capture_stream[64] = {};
+
+std::vector<uintptr_t> graph_key(const qgemv_stack_layer* layers, const qgemv_stack_shape* shape,
+                                 const uint16_t* x, const uint16_t* y, const void* workspace,
+                                 int dev) {
+  std::vector<uintptr_t> k;
+  const int NL = shape->n_layers;
+  k.reserve(12 + static_cast<size_t>(NL) * (sizeof(qgemv_stack_layer) / sizeof(uintptr_t) + 1));
+  uint32_t eps_bits;
+  memcpy(&eps_bits, &shape->eps, sizeof(eps_bits));
+  const uintptr_t head[] = {static_cast<uintptr_t>(dev),          static_cast<uintptr_t>(shape->hidden),
+                            static_cast<uintptr_t>(shape->n_q),   static_cast<uintptr_t>(shape->n_kv),
+                            static_cast<uintptr_t>(shape->head_dim), static_cast<uintptr_t>(shape->inter),
+                            static_cast<uintptr_t>(NL),           eps_bits,
+                            reinterpret_cast<uintptr_t>(x),       reinterpret_cast<uintptr_t>(y),
+                            reinterpret_cast<uintptr_t>(workspace)};
+  k.insert(k.end(), head, head + sizeof(head) / sizeof(head[0]));
+  for (int l = 0; l < NL; ++l) {
+    const qgemv_stack_layer& s = layers[l];
+    const void* p[17] = {s.qkv_codes,   s.qkv_scales,  s.qkv_biases,  s.attn_norm,  s.o_codes,
+                         s.o_scales,    s.o_biases,    s.gate_codes,  s.gate_scales,
+                         s.gate_biases, s.up_codes,    s.up_scales,   s.up_biases,  s.mlp_norm,
+                         s.down_codes,  s.down_scales, s.down_biases};
+    for (const void* q : p) k.push_back(reinterpret_cast<uintptr_t>(q));
+  }
+  return k;
+}
+
+// Capture the call's launches into a graph instance (nullptr on failure;
+// the caller then launches eagerly).
+cudaGraphExec_t capture_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape* shape,
+                              const uint16_t* x, uint16_t* y, void* workspace, int dev, int sms) {
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (g_capture_stream[dev] == nullptr &&
+      cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    g_capture_stream[dev] = nullptr;
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaStream_t cap = g_capture_stream[dev];
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  const int rc = enqueue_stack(layers, shape, x, y, workspace, dev, sms, cap);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(cap, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (rc == QGEMV_OK && e == cudaSuccess && graph != nullptr &&
+      cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    exec = nullptr;
+  if (graph != nullptr) cudaGraphDestroy(graph);
+  cudaGetLastError();  // a failed capture leaves no sticky error behind
+  return exec;
+}
 
 }  // namespace
 
@@ -74,9 +158,58 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return QGEMV_EDEVICE;
+  // Each op must take the streaming kernel (K a multiple of 1024, at most 16384).
+  if (!make_stream_plan(kNorm, 4, H, nqkv, 1, sms).ok ||
+      !make_stream_plan(kPlain, 4, Dq, H, 1, sms).ok ||
+      !make_stream_plan(kSwiglu, 4, H, I, 1, sms).ok ||
+      !make_stream_plan(kPlain, 4, I, H, 1, sms).ok)
+    return QGEMV_EINVAL;
 
-  // The four ops' plans (the same for every layer); each must take the
-  // streaming kernel (K a multiple of 1024, at most 16384).
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // A caller that is capturing its own graph gets the launches themselves.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return QGEMV_ELAUNCH;
+  }
+  if (cs != cudaStreamCaptureStatusNone)
+    return enqueue_stack(layers, shape, x, y, workspace, dev, sms, st);
+
+  const std::vector<uintptr_t> key = graph_key(layers, shape, x, y, workspace, dev);
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  GraphEntry* hit = nullptr;
+  for (GraphEntry& g : g_graphs)
+    if (g.exec != nullptr && g.key == key) hit = &g;
+  if (hit == nullptr) {
+    cudaGraphExec_t exec = capture_stack(layers, shape, x, y, workspace, dev, sms);
+    if (exec == nullptr) return enqueue_stack(layers, shape, x, y, workspace, dev, sms, st);
+    GraphEntry* victim = &g_graphs[0];
+    for (GraphEntry& g : g_graphs)
+      if (g.exec == nullptr || g.last_use < victim->last_use) victim = &g;
+    if (victim->exec != nullptr) cudaGraphExecDestroy(victim->exec);
+    victim->exec = exec;
+    victim->key = key;
+    hit = victim;
+  }
+  hit->last_use = ++g_graph_clock;
+  if (cudaGraphLaunch(hit->exec, st) != cudaSuccess) return QGEMV_ELAUNCH;
+  return QGEMV_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int enqueue_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape* shape,
+                  const uint16_t* x, uint16_t* y, void* workspace, int dev, int sms,
+                  cudaStream_t st) {
+  using namespace qgemv;
+  const int H = shape->hidden, nq = shape->n_q, nkv = shape->n_kv, hd = shape->head_dim;
+  const int I = shape->inter, NL = shape->n_layers;
+  const int Dq = nq * hd;
+  const int nqkv = (nq + 2 * nkv) * hd;
+
+  // The four ops' plans (the same for every layer).
   const StreamPlan p0 = make_stream_plan(kNorm, 4, H, nqkv, 1, sms);
   const StreamPlan p1 = make_stream_plan(kPlain, 4, Dq, H, 1, sms);
   const StreamPlan p2 = make_stream_plan(kSwiglu, 4, H, I, 1, sms);
@@ -96,7 +229,6 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   wp += up256(2 * static_cast<size_t>(H));
   xbuf[1] = reinterpret_cast<__half*>(wp);
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto hp = [](const uint16_t* p) { return reinterpret_cast<const __half*>(p); };
   auto cp = [](const uint32_t* p) { return reinterpret_cast<const uint8_t*>(p); };
   for (int l = 0; l < NL; ++l) {
@@ -164,4 +296,4 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
   return QGEMV_OK;
 }
 
-}  // extern "C"
+}  // namespace

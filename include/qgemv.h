@@ -240,7 +240,11 @@ size_t qgemv_decode_stack_workspace_bytes(const qgemv_stack_shape *shape);
  * most 16384, eps > 0.  Enqueues 4 * n_layers streaming-kernel launches on
  * `stream` (programmatic dependent launch between them: each op's weights
  * start streaming while the previous op finishes); calls that share a
- * workspace must not overlap on the GPU.
+ * workspace must not overlap on the GPU.  The launches of each distinct
+ * argument set (device, shape, every pointer) are captured once into a
+ * CUDA graph (up to 4 kept, least recently used replaced) and later calls
+ * replay it with one graph launch on `stream`; when `stream` is itself
+ * being captured, the launches are enqueued on it directly.
  */
 int qgemv_decode_stack(const qgemv_stack_layer *layers, const qgemv_stack_shape *shape,
                        const uint16_t *x, uint16_t *y, void *workspace, size_t workspace_bytes,

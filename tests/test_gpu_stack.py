@@ -87,3 +87,35 @@ def test_stack_rejects_bad_shapes():
         with pytest.raises(q.QgemvError):
             q.decode_stack(layers, bad, x, workspace=torch.empty(1 << 20, dtype=torch.uint8,
                                                                   device="cuda"))
+
+
+def test_stack_graph_cache_and_caller_capture():
+    """Repeated calls replay a cached graph; more distinct argument sets than
+    the cache holds, and a call inside the caller's own stream capture, give
+    the same bits as the first (captured) call."""
+    H, nq, nkv, hd, I, NL = 1024, 8, 2, 128, 2048, 2
+    layers, _ = make_layers(402, NL, H, nq, nkv, hd, I)
+    sh = q.stack_shape(H, nq, nkv, hd, I, NL, 1e-5)
+    arr = q.stack_layers(layers)
+    x = dev16(synth.activation(synth.rng(402, H, synth.TID["x"]), H))
+    ws = torch.empty(q.decode_stack_workspace_bytes(sh), dtype=torch.uint8, device="cuda")
+    ref = q.decode_stack(arr, sh, x, workspace=ws).clone()
+    ys = [torch.empty(H, dtype=torch.float16, device="cuda") for _ in range(6)]
+    for rep in range(2):                       # 6 keys > 4 cached: evictions, then re-captures
+        for y in ys:
+            q.decode_stack(arr, sh, x, y=y, workspace=ws)
+            torch.cuda.synchronize()
+            assert torch.equal(y, ref), rep
+    y = torch.empty(H, dtype=torch.float16, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            q.decode_stack(arr, sh, x, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    assert q.device_status() == 0
