@@ -42,12 +42,13 @@ int enqueue_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape* shap
                   cudaStream_t st);
 
 // CUDA-graph cache of the decode stack.  A call enqueues 4 * n_layers
-// kernels; on the Grace host of a GB300 node a cudaLaunchKernelEx costs about
-// 8 us of host time, close to an op's device time, so eager launches bound a
-// 32-layer token by the host (~1050 us).  Each distinct argument set (device,
-// shape, every pointer) is therefore captured once into a graph whose
-// instance later calls replay with one cudaGraphLaunch (~2 us of host time).
-// The kernels and their programmatic dependencies are the same either way.
+// kernels; issued eagerly and back to back, a 32-layer call on a GB300 node
+// held its host thread for ~1050 us (as long as the GPU work, ~1075 us), so
+// the host could not run ahead.  Each distinct argument set (device, shape,
+// every pointer) is therefore captured once into a graph whose instance
+// later calls replay with one cudaGraphLaunch (~9 us of host time per call
+// back to back, ~18 us into an idle stream).  The kernels and their
+// programmatic dependencies are the same either way.
 constexpr int kGraphCacheSize = 4;
 
 struct GraphEntry {
