@@ -58,6 +58,10 @@ def parse_args():
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, lm_head, gemv1024, qwen_stack, "
                         "w2_layer, m2, m4, m8, m8_w2, or all")
+    p.add_argument("--copies", type=int, default=0,
+                   help="--op: device copies of the weights to rotate through (default: "
+                        "enough to exceed 3x L2; 1 keeps them resident in L2, the "
+                        "compute-only variant)")
     return p.parse_args()
 
 
@@ -428,8 +432,9 @@ OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "gemv1024", "qwen_st
 
 def run_op(args):
     """One op (or one workload configuration's unit of work) timed alone:
-    a CUDA graph of calls on rotating device copies (more bytes than L2),
-    replayed; one JSON line per op.  `--op all` runs every entry of OPS."""
+    a CUDA graph of at least 32 calls on rotating device copies of the
+    weights (more bytes than L2 unless `--copies` says otherwise), replayed;
+    one JSON line per op.  `--op all` runs every entry of OPS."""
     names = OPS if args.op == "all" else [args.op]
     for name in names:
         run_one_op(args, name)
@@ -587,7 +592,10 @@ def run_one_op(args, name):
     copies = 1 if name == "qwen_stack" else max(2, int(3 * 129e6 // max(weight_bytes, 1)) + 1)
     if name == "gemv1024":
         copies = max(copies, 512)
+    if args.copies > 0 and name != "qwen_stack":
+        copies = args.copies
     ws = [base] + [tuple(tuple(t.clone() for t in wt) for wt in base) for _ in range(copies - 1)]
+    n_graph = max(copies, 32)  # calls per captured graph, cycling over the copies
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -600,17 +608,17 @@ def run_one_op(args, name):
     if graph:
         cg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cg):
-            for i in range(copies):
-                call(ws[i])
-        reps = max(1, args.steps // copies)
-        for _ in range(max(3, args.warmup // copies)):
+            for i in range(n_graph):
+                call(ws[i % copies])
+        reps = max(1, args.steps // n_graph)
+        for _ in range(max(3, args.warmup // n_graph)):
             cg.replay()
         torch.cuda.synchronize()
         e0.record()
         for _ in range(reps):
             cg.replay()
         e1.record()
-        n_calls = reps * copies
+        n_calls = reps * n_graph
     else:
         reps = max(1, min(args.steps, 300))
         for i in range(max(3, min(args.warmup, 20))):
@@ -630,7 +638,9 @@ def run_one_op(args, name):
                       else "achieved HBM GB/s of one unit (stream launches)",
                       "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 3),
                       "bytes_per_call": nbytes, "launches_per_call": launches,
-                      "weight_copies": copies, "calls_timed": n_calls, "peak": peak,
+                      "weight_copies": copies,
+                      "l2_resident": bool(copies * max(weight_bytes, nbytes) < 129e6),
+                      "calls_timed": n_calls, "peak": peak,
                       "peak_kind": peak_kind, "frac": round(gbs / peak, 4),
                       "device_status": q.device_status()}), flush=True)
 
