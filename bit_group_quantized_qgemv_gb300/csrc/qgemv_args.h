@@ -173,7 +173,9 @@ inline StreamPlan make_batch_plan(int bits, int K, long long rows, int M, int sm
   int s = target / tg;
   if (s < 1) s = 1;
   const int t = s * tg;
-  int jr = (mb == 2) ? 4 : 2;
+  // 4 rows per slot and stage (2 for MB = 4 and 8 measured 8-12 % slower on
+  // GB300: the per-stage handshake and reduction over fewer FMAs)
+  int jr = 4;
   const int task_bytes = K * bits / 8 + 2 * (K / 32);
   while (jr > 1 && static_cast<long long>(s) * jr * task_bytes > stage_limit) jr /= 2;
   const int rs = s * jr;

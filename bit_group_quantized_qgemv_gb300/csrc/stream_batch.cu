@@ -356,9 +356,11 @@ cudaError_t launch_batch_bits(const StreamPlan& p, const StreamArgs& a, cudaStre
     return launch_batch_t<BITS, 2, 32, 1>(p, a, st, device);
   }
   if (p.mb == 4) {
+    if (p.jr == 4) return launch_batch_t<BITS, 4, 32, 4>(p, a, st, device);
     if (p.jr == 2) return launch_batch_t<BITS, 4, 32, 2>(p, a, st, device);
     return launch_batch_t<BITS, 4, 32, 1>(p, a, st, device);
   }
+  if (p.jr == 4) return launch_batch_t<BITS, 8, 16, 4>(p, a, st, device);
   if (p.jr == 2) return launch_batch_t<BITS, 8, 16, 2>(p, a, st, device);
   return launch_batch_t<BITS, 8, 16, 1>(p, a, st, device);
 }
