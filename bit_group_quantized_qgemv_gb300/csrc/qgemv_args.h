@@ -168,14 +168,16 @@ inline StreamPlan make_batch_plan(int bits, int K, long long rows, int M, int sm
   const int kpt = (mb == 8) ? 16 : 32;
   if (K % (32 * kpt) != 0) return p;
   const int tg = K / kpt;
-  const int target = (mb == 2) ? 512 : 256;
+  const int target = 256;
   if (tg > (mb == 8 ? 256 : (mb == 4 ? 448 : 512))) return p;  // the kernels' launch bounds
   int s = target / tg;
   if (s < 1) s = 1;
   const int t = s * tg;
-  // 4 rows per slot and stage (2 for MB = 4 and 8 measured 8-12 % slower on
-  // GB300: the per-stage handshake and reduction over fewer FMAs)
-  int jr = 4;
+  // Rows per slot and stage: 8 for MB = 2, 4 for MB = 4 and 8 (measured on
+  // GB300: 2 rows for MB = 4 / 8 was 8-12 % slower, the per-stage handshake
+  // and reduction spread over fewer FMAs; MB = 2 with 512 threads of 4 rows
+  // 3 % slower; MB = 4 with 8 rows spills)
+  int jr = (mb == 2) ? 8 : 4;
   const int task_bytes = K * bits / 8 + 2 * (K / 32);
   while (jr > 1 && static_cast<long long>(s) * jr * task_bytes > stage_limit) jr /= 2;
   const int rs = s * jr;

@@ -351,6 +351,7 @@ template <int BITS>
 cudaError_t launch_batch_bits(const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                               int device) {
   if (p.mb == 2) {
+    if (p.jr == 8) return launch_batch_t<BITS, 2, 32, 8>(p, a, st, device);
     if (p.jr == 4) return launch_batch_t<BITS, 2, 32, 4>(p, a, st, device);
     if (p.jr == 2) return launch_batch_t<BITS, 2, 32, 2>(p, a, st, device);
     return launch_batch_t<BITS, 2, 32, 1>(p, a, st, device);
