@@ -177,10 +177,14 @@ __device__ __forceinline__ float task_dot(const uint8_t* codes, const uint32_t* 
 // (the kernels multiply fp16 activations) and packed in the pairing of the
 // code lanes (4-bit: (x_{8i+j}, x_{8i+j+4}); 2-bit: (x_{16i+j}, x_{16i+j+8})),
 // plus their sum times 2^-24 (the dot products' scale).  16-byte aligned.
+// gpre: gamma[k0 .. k0 + KPT) already loaded (load_gamma), else read here;
+// sq (optional) receives the sum of squares of the raw x (for RMSNorm).
 template <int BITS, int KPT>
 __device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma, const float* xf,
-                                            int k0, uint32_t (&xp)[KPT / 2], float& xs_scaled) {
+                                            int k0, uint32_t (&xp)[KPT / 2], float& xs_scaled,
+                                            const uint4* gpre = nullptr, float* sq = nullptr) {
   float part[KPT / 16];
+  float sqa = 0.f;
 #pragma unroll
   for (int c = 0; c < KPT / 16; ++c) {  // 16 activations at a time
     float xv[16];
@@ -198,7 +202,10 @@ __device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma
       const uint4* src = reinterpret_cast<const uint4*>(x + k0 + 16 * c);
       uint4 raw[2] = {src[0], src[1]};
       uint4 graw[2];
-      if (gamma != nullptr) {
+      if (gpre != nullptr) {
+        graw[0] = gpre[2 * c];
+        graw[1] = gpre[2 * c + 1];
+      } else if (gamma != nullptr) {
         const uint4* g = reinterpret_cast<const uint4*>(gamma + k0 + 16 * c);
         graw[0] = g[0];
         graw[1] = g[1];
@@ -209,6 +216,7 @@ __device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           float2 f = __half22float2(h[j]);
+          if (sq != nullptr) sqa = fmaf(f.x, f.x, fmaf(f.y, f.y, sqa));
           if (gamma != nullptr) {
             const float2 gf = __half22float2(reinterpret_cast<const __half2*>(&graw[i])[j]);
             f.x *= gf.x;
@@ -244,26 +252,16 @@ __device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma
 #pragma unroll
   for (int c = 0; c < KPT / 16; ++c) sum += part[c];
   xs_scaled = sum * kTwoM24;
+  if (sq != nullptr) *sq = sqa;
 }
 
-// 1 / sqrt(mean(x^2) + eps) of an fp16 vector of length K (a multiple of
-// 256), computed by one warp with 16-byte loads; every lane returns it.
-__device__ __forceinline__ float warp_rstd(const __half* x, int K, float eps, int lane) {
-  float sq = 0.f;
-  const uint4* v = reinterpret_cast<const uint4*>(x);
-#pragma unroll 4
-  for (int i = lane; i < K / 8; i += 32) {
-    const uint4 raw = v[i];
-    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+// gamma[k0 .. k0 + KPT) into registers (a weight: no kernel writes it, so
+// it may be read before the previous kernel's grid has completed).
+template <int KPT>
+__device__ __forceinline__ void load_gamma(const __half* gamma, int k0, uint4 (&g)[KPT / 8]) {
+  const uint4* src = reinterpret_cast<const uint4*>(gamma + k0);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __half22float2(h[j]);
-      sq = fmaf(f.x, f.x, fmaf(f.y, f.y, sq));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  return 1.0f / sqrtf(sq / static_cast<float>(K) + eps);
+  for (int i = 0; i < KPT / 8; ++i) g[i] = src[i];
 }
 
 template <int BITS, int MODE, int JR, int KPT>
@@ -277,6 +275,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   __shared__ __align__(8) uint64_t xready_bar;  // every consumer warp has its activations
   __shared__ int s_eidx[kMaxTopK];
   __shared__ float s_ewt[kMaxTopK];
+  __shared__ float s_sq[16];  // RMSNorm modes: sums of x^2 of slot 0's consumer warps
 
   const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
@@ -394,16 +393,24 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   const int red_stage = (tasks * wpt + 3) & ~3;  // floats, 16-byte multiple
 
   if (epi) {
-    // Epilogue warp: RMS of the input (RMSNorm modes), then finish every
-    // stage's rows once all partials are in.  It reads x and residuals and
-    // writes y, so it waits for the previous kernel first.
+    // Epilogue warp: finish every stage's rows once all partials are in
+    // (the RMS of the input, RMSNorm modes, from the consumers' sums of
+    // squares).  It reads residuals and writes y, so it waits for the
+    // previous kernel first.
     pdl_wait();
-    const float rstd = use_gamma ? warp_rstd(a.x, a.K, a.eps, lane) : 1.f;
+    float rstd = 1.f;
+    bool have_rstd = !use_gamma;
     for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
       const int n = wk.rows();
       const int s = wk.slot;
       const int row = wk.row;
       if (!mbar_wait(smem_u32(&part_bar[s]), wk.phase, &g_status)) return;
+      if (!have_rstd) {  // slot 0's warps stored their sums of x^2 before arriving
+        float tot = 0.f;
+        for (int w = 0; w < wpt; ++w) tot += s_sq[w];
+        rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+        have_rstd = true;
+      }
       const bool ok = (MODE == kMoeUp) ? (s_eidx[wk.expert_slot] >= 0) : true;
       const float* rs = red + static_cast<size_t>(s) * red_stage;
       for (int r = lane; r < n; r += 32) {
@@ -450,6 +457,8 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   // block-wide staging or barrier, so each warp starts on its own.
   uint32_t xp[TK::kXRegs];
   float xs_scaled;
+  uint4 gpre[KPT / 8];
+  if (use_gamma) load_gamma<KPT>(a.gamma, uu * KPT, gpre);  // before the wait: a weight
   pdl_wait();  // x may come from the previous kernel
   if (MODE == kMoeDown)
     load_task_x<BITS, KPT>(nullptr, nullptr, a.xf + static_cast<size_t>(ek) * a.K, uu * KPT, xp,
@@ -463,8 +472,16 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
                   a.gather_hd +
         (k0 - head * a.gather_hd);
     load_task_x<BITS, KPT>(src, nullptr, nullptr, 0, xp, xs_scaled);
+  } else if (use_gamma) {
+    float sq;
+    load_task_x<BITS, KPT>(a.x, a.gamma, nullptr, uu * KPT, xp, xs_scaled, gpre, &sq);
+    if (slot == 0) {  // slot 0's threads cover K once: its warps' sums give mean(x^2)
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (lane == 0) s_sq[wit] = sq;
+    }
   } else {
-    load_task_x<BITS, KPT>(a.x, use_gamma ? a.gamma : nullptr, nullptr, uu * KPT, xp, xs_scaled);
+    load_task_x<BITS, KPT>(a.x, nullptr, nullptr, uu * KPT, xp, xs_scaled);
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&xready_bar));
