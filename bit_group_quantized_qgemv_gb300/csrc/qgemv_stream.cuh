@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
   __shared__ int s_eidx[kMaxTopK];
   __shared__ float s_ewt[kMaxTopK];
   __shared__ float s_sq[16];  // RMSNorm modes: sums of x^2 of slot 0's consumer warps
+  __shared__ float s_res[64];  // residual rows of a CTA's row band (at most 64 rows)
 
   const int T = static_cast<int>(blockDim.x) - 64;  // consumer threads
   const int warp = threadIdx.x >> 5;
@@ -400,6 +401,14 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     pdl_wait();
     float rstd = 1.f;
     bool have_rstd = !use_gamma;
+    // A contiguous band of at most 64 rows: load its residual rows now, so
+    // the last stage's tail does not wait for them.
+    const bool res_pre = (MODE == kPlain || MODE == kMoeDown) && a.residual != nullptr &&
+                         !a.interleave && r1 - r0 <= 64;
+    if (res_pre) {
+      for (int i = lane; i < r1 - r0; i += 32) s_res[i] = __half2float(a.residual[r0 + i]);
+      __syncwarp();
+    }
     for (StageWalker wk(r0, r1, a.RS, NS, rpe, stride); wk.more();) {
       const int n = wk.rows();
       const int s = wk.slot;
@@ -434,7 +443,10 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
         for (int m = 0; m < NMAT; ++m) v[m] *= kTwo24;
         if (MODE == kPlain || MODE == kMoeDown) {
           float o = v[0];
-          if (a.residual != nullptr) o += __half2float(a.residual[gr]);
+          if (res_pre)
+            o += s_res[gr - r0];
+          else if (a.residual != nullptr)
+            o += __half2float(a.residual[gr]);
           a.y[gr] = __float2half_rn(o);
         } else if (MODE == kNorm) {
           a.y[gr] = __float2half_rn(v[0] * rstd);
