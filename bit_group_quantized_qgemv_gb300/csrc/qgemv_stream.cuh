@@ -400,7 +400,14 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     // previous kernel first.
     pdl_wait();
     float rstd = 1.f;
-    bool have_rstd = !use_gamma;
+    if (use_gamma) {
+      // Slot 0's warps store their sums of x^2 before arriving on xready,
+      // so the RMS is ready while the first stage is being computed.
+      if (!mbar_wait(smem_u32(&xready_bar), 0, &g_status)) return;
+      float tot = 0.f;
+      for (int w = 0; w < wpt; ++w) tot += s_sq[w];
+      rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+    }
     // A contiguous band of at most 64 rows: load its residual rows now, so
     // the last stage's tail does not wait for them.
     const bool res_pre = (MODE == kPlain || MODE == kMoeDown) && a.residual != nullptr &&
@@ -414,12 +421,6 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       const int s = wk.slot;
       const int row = wk.row;
       if (!mbar_wait(smem_u32(&part_bar[s]), wk.phase, &g_status)) return;
-      if (!have_rstd) {  // slot 0's warps stored their sums of x^2 before arriving
-        float tot = 0.f;
-        for (int w = 0; w < wpt; ++w) tot += s_sq[w];
-        rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
-        have_rstd = true;
-      }
       const bool ok = (MODE == kMoeUp) ? (s_eidx[wk.expert_slot] >= 0) : true;
       const float* rs = red + static_cast<size_t>(s) * red_stage;
       for (int r = lane; r < n; r += 32) {
