@@ -464,7 +464,9 @@ def run_op(args):
     """One op (or one workload configuration's unit of work) timed alone:
     a CUDA graph of at least 32 calls on rotating device copies of the
     weights (more bytes than L2 unless `--copies` says otherwise), replayed;
-    one JSON line per op.  `--op all` runs every entry of OPS."""
+    one JSON line per op: the mean over all replays (`us_per_call`) and
+    p10 / p50 / p90 of 100-200 replays timed one by one (`us_per_call_pct`,
+    per call).  `--op all` runs every entry of OPS."""
     names = OPS if args.op == "all" else [args.op]
     for name in names:
         run_one_op(args, name)
@@ -649,6 +651,13 @@ def run_one_op(args, name):
             cg.replay()
         e1.record()
         n_calls = reps * n_graph
+        # Distribution: events around each of up to 200 further replays.
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(200, max(100, reps)))]
+        for a_, b_ in pev:
+            a_.record()
+            cg.replay()
+            b_.record()
     else:
         reps = max(1, min(args.steps, 300))
         for i in range(max(3, min(args.warmup, 20))):
@@ -659,14 +668,24 @@ def run_one_op(args, name):
             call(ws[0])
         e1.record()
         n_calls = reps
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(100)]
+        for a_, b_ in pev:
+            a_.record()
+            call(ws[0])
+            b_.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / n_calls
+    per = sorted(a_.elapsed_time(b_) / (n_graph if graph else 1) for a_, b_ in pev)
+    pct = {"p10": round(per[len(per) // 10] * 1e3, 3), "p50": round(per[len(per) // 2] * 1e3, 3),
+           "p90": round(per[(9 * len(per)) // 10] * 1e3, 3), "replays": len(per)}
     peak, peak_kind = measured_peak()
     gbs = nbytes / (ms * 1e-3) / 1e9
     print(json.dumps({"op": name, "config": config,
                       "metric": "achieved HBM GB/s of one unit (CUDA-graph replays)" if graph
                       else "achieved HBM GB/s of one unit (stream launches)",
                       "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 3),
+                      "us_per_call_pct": pct,
                       "bytes_per_call": nbytes, "launches_per_call": launches,
                       "weight_copies": copies,
                       "l2_resident": bool(copies * max(weight_bytes, nbytes) < 129e6),
