@@ -69,6 +69,16 @@ def parse_args():
     return p.parse_args()
 
 
+def max_over_ranks(torch, values, device, world):
+    """Each rank's timings -> their maximum over all ranks (the job's time,
+    since every rank must finish); identity on one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
@@ -372,10 +382,7 @@ def run_own(args):
     swiglu_bytes = dict(ops)["gate_up_swiglu"]
     status = q.device_status()
 
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks(torch, [ms, ms_e2e], device, world)
 
     peak, peak_kind = measured_peak()
     value = world * step_bytes * K / (ms * 1e-3) / 1e9
