@@ -193,7 +193,16 @@ int qgemv_decode_stack(const qgemv_stack_layer* layers, const qgemv_stack_shape*
     hit = victim;
   }
   hit->last_use = ++g_graph_clock;
-  if (cudaGraphLaunch(hit->exec, st) != cudaSuccess) return QGEMV_ELAUNCH;
+  if (cudaGraphLaunch(hit->exec, st) != cudaSuccess) {
+    // A cached instance that no longer launches (its context was reset, say)
+    // is dropped; this call launches eagerly and the next one re-captures.
+    cudaGetLastError();
+    cudaGraphExecDestroy(hit->exec);
+    cudaGetLastError();
+    hit->exec = nullptr;
+    hit->key.clear();
+    return enqueue_stack(layers, shape, x, y, workspace, dev, sms, st);
+  }
   return QGEMV_OK;
 }
 
