@@ -119,3 +119,27 @@ def test_stack_graph_cache_and_caller_capture():
     torch.cuda.synchronize()
     assert torch.equal(y, ref)
     assert q.device_status() == 0
+
+
+def test_bench_configuration_32_layers():
+    """The configuration bench.py times: 32 device copies of one
+    Llama-3.1-8B-shaped layer and the benchmark's input, one
+    qgemv_decode_stack call.  The chain of single-op calls' last down
+    projection is checked against the oracle on its own fp16 inputs
+    (stage-isolated), and the stack's output against the chain within that
+    projection's tolerance."""
+    import bench
+    c = synth.LLAMA8B
+    layers, x0, _ = bench.build_stack(torch, 32, torch.device("cuda", 0))
+    sh = q.stack_shape(c["hidden"], c["n_q"], c["n_kv"], c["head_dim"], c["inter"], 32, c["eps"])
+    y = q.decode_stack(layers, sh, x0)
+    y_chain, act, h = chain(layers, x0, c["n_q"], c["n_kv"], c["head_dim"], c["eps"])
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y.float()).all())
+    down = synth.llama_layer(1, 0, 4)["down"]
+    y64, _, bound = oracle.qgemv(4, down.codes, down.scales, down.biases, act.cpu().numpy(),
+                                 h.cpu().numpy())
+    check(y_chain, y64, plain_tol(bound), "bench configuration: chain's last down vs oracle")
+    check(y, y_chain.double().cpu().numpy(), plain_tol(bound),
+          "bench configuration: stack vs single-op chain")
+    assert q.device_status() == 0
