@@ -12,6 +12,14 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 
 
+def pytest_sessionstart(session):
+    # Every test module imports the package, which loads libqgemv.so, at
+    # collection; a fresh checkout has not built it (nor the C oracle) yet.
+    # The build is incremental: a no-op when both are up to date.
+    import __graft_entry__
+    __graft_entry__.build()
+
+
 def load_golden(name):
     """Parse a tests/golden/*.txt fixture into a dict of strings."""
     out = {}
