@@ -60,8 +60,8 @@ def parse_args():
                    help="skip the single-op CUDA-graph comparison")
     p.add_argument("--op", default="stack",
                    help="time one op or configuration unit alone instead of the stack: "
-                        "qkv, o_proj, swiglu, down, moe, lm_head, gemv1024, qwen_stack, "
-                        "w2_layer, m2, m4, m8, m8_w2, or all")
+                        "qkv, o_proj, swiglu, down, moe, lm_head, lm_head_argmax, gemv1024, "
+                        "qwen_stack, w2_layer, m2, m4, m8, m8_w2, or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
                         "enough to exceed 3x L2; 1 keeps them resident in L2, the "
@@ -469,8 +469,8 @@ def run_own(args):
     return 0
 
 
-OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "gemv1024", "qwen_stack",
-       "w2_layer", "m2", "m4", "m8", "m8_w2"]
+OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "lm_head_argmax", "gemv1024",
+       "qwen_stack", "w2_layer", "m2", "m4", "m8", "m8_w2"]
 
 
 def run_op(args):
@@ -549,9 +549,13 @@ def run_one_op(args, name):
         def call(w):
             q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y, workspace=work)
         launches = 2
-    elif name in ("lm_head", "gemv1024"):
+    elif name in ("lm_head", "lm_head_argmax", "gemv1024"):
         if name == "lm_head":
             config = "config 2: Qwen3-0.6B-shaped lm_head 1024->151936"
+            N, K, wl = cq["vocab"], cq["hidden"], 2
+        elif name == "lm_head_argmax":
+            config = ("config 2: Qwen3-0.6B-shaped lm_head 1024->151936 with the greedy token "
+                      "chosen on the GPU")
             N, K, wl = cq["vocab"], cq["hidden"], 2
         else:
             config = "config 0: single 4-bit g64 GEMV 1024x1024"
@@ -561,9 +565,14 @@ def run_one_op(args, name):
         nbytes = acc.matvec_bytes(N, K, 4)
         x = torch.from_numpy(synth.activation(synth.rng(wl, 0, synth.TID["x"]), K)).to(dev)
         y = torch.empty(N, device=dev).half()
+        am_scratch = torch.zeros(q.argmax_scratch_bytes(), dtype=torch.uint8, device=dev)
+        am_token = torch.empty(1, dtype=torch.int32, device=dev)
 
         def call(w):
-            q.qgemv_w4g64(w[0], x, y=y)
+            if name == "lm_head_argmax":
+                q.lm_head_argmax(w[0], x, logits=y, scratch=am_scratch, token=am_token)
+            else:
+                q.qgemv_w4g64(w[0], x, y=y)
         launches = 1
     elif name == "w2_layer":
         config = "config 4: the five matvecs of one 8B-shaped layer at 2-bit"

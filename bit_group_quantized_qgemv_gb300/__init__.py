@@ -17,6 +17,8 @@ from ._binding import (  # noqa: F401
     device_status,
     last_cuda_error,
     lib,
+    lm_head_argmax,
+    argmax_scratch_bytes,
     moe_qgemv_combine,
     moe_qgemv_combine_noalloc,
     noalloc_max_scratch_bytes,

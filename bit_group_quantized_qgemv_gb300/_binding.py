@@ -38,6 +38,8 @@ _SIGS = {
     "qgemv_device_status": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "qgemv_version": (_I, []),
     "qgemv_selftest_wait_timeout": (_I, [ctypes.c_uint, ctypes.c_void_p]),
+    "qgemv_lm_head_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
+    "qgemv_argmax_scratch_bytes": (ctypes.c_size_t, []),
 }
 
 #: Names the C header declares (the binding exposes each one).
@@ -132,6 +134,34 @@ def qgemv_w4g64(w, x, y=None, residual=None, stream=None):
 def qgemv_w2g64(w, x, y=None, residual=None, stream=None):
     """y = W x (+ residual) for a 2-bit g64 weight w = (codes, scales, biases)."""
     return _plain(lib.qgemv_w2g64, 2, w, x, y, residual, stream)
+
+
+def argmax_scratch_bytes() -> int:
+    return int(lib.qgemv_argmax_scratch_bytes())
+
+
+def lm_head_argmax(w, x, logits=None, scratch=None, token=None, stream=None):
+    """Greedy lm_head (qgemv_lm_head_argmax): logits = W x (4-bit g64) and
+    token = the lowest index of the largest logit, both on the device.
+    `scratch` (uint8, argmax_scratch_bytes(), zero before first use; left
+    zero) may be kept across calls; a fresh zeroed one is made if None.
+    Returns (token int32 [1], logits fp16 [N])."""
+    codes, scales, biases = _weight(w, "w")
+    x = _cuda(x, _F16, "x")
+    N = codes.shape[-2]
+    K = codes.shape[-1] * 8  # 4-bit: 8 codes per 32-bit word
+    if logits is None:
+        logits = torch.empty(N, dtype=torch.float16, device=x.device)
+    if scratch is None:
+        scratch = torch.zeros(argmax_scratch_bytes(), dtype=torch.uint8, device=x.device)
+    if token is None:
+        token = torch.empty(1, dtype=torch.int32, device=x.device)
+    _cuda(logits, _F16, "logits")
+    _cuda(token, (torch.int32,), "token")
+    st = lib.qgemv_lm_head_argmax(_ptr(codes), _ptr(scales), _ptr(biases), _ptr(x), _ptr(logits),
+                                  N, K, _ptr(scratch), _ptr(token), _stream(stream))
+    _check(st, "qgemv_lm_head_argmax")
+    return token, logits
 
 
 def rmsnorm_qgemv(w, x, norm_weight, eps=1e-5, y=None, stream=None):

@@ -300,6 +300,41 @@ int qgemv_device_status(unsigned* flags) {
   return QGEMV_OK;
 }
 
+size_t qgemv_argmax_scratch_bytes(void) { return 16; }
+
+int qgemv_lm_head_argmax(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                         const uint16_t* x, uint16_t* logits, int N, int K, void* scratch,
+                         int32_t* token, void* stream) {
+  if (!codes || !scales || !biases || !x || !logits || !scratch || !token) return QGEMV_ENULL;
+  if (N < 1 || !valid_k(K)) return QGEMV_EINVAL;
+  if (!aligned(codes, 4) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(x, 2) ||
+      !aligned(logits, 2) || !aligned(scratch, 8) || !aligned(token, 4))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  StreamArgs a = blank_args();
+  a.codes[0] = reinterpret_cast<const uint8_t*>(codes);
+  a.scales[0] = reinterpret_cast<const __half*>(scales);
+  a.biases[0] = reinterpret_cast<const __half*>(biases);
+  a.x = reinterpret_cast<const __half*>(x);
+  a.y = reinterpret_cast<__half*>(logits);
+  a.rows = N;
+  a.K = K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, 4, K, N, 1, sms);
+  if (p.ok && aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
+      aligned(x, 16)) {
+    a.am_key = static_cast<unsigned long long*>(scratch);
+    const cudaError_t e = qgemv::stream_argmax(p, a, st, dev);
+    if (e != cudaSuccess) return finish(e);
+    return finish(qgemv::argmax_finalize_launch(a.am_key, token, st));
+  }
+  // Other shapes: the generic GEMV, then a one-CTA argmax over the logits.
+  const cudaError_t e = qgemv::generic_launch(qgemv::kPlain, 4, a, st);
+  if (e != cudaSuccess) return finish(e);
+  return finish(qgemv::argmax_launch(a.y, N, token, st));
+}
+
 int qgemv_selftest_wait_timeout(unsigned limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return QGEMV_EINVAL;
   int dev = 0, sms = 0;

@@ -223,6 +223,52 @@ cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n
   return cudaLaunchKernelEx(&cfg, attention_seq1_kernel, qkv, out, n_q, n_kv, head_dim);
 }
 
+// Argmax of an fp16 vector by one CTA of 1024 threads (lowest index of the
+// largest value, the same key as the streaming kernel's kArgmax epilogue).
+__global__ void __launch_bounds__(1024) argmax_kernel(const __half* __restrict__ y, int n,
+                                                      int* __restrict__ token) {
+  __shared__ unsigned long long s_best[32];
+  unsigned long long best = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    best = max_key(best, argmax_key(__half2float(y[i]), i));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) best = max_key(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if ((threadIdx.x & 31) == 0) s_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    best = threadIdx.x < blockDim.x / 32 ? s_best[threadIdx.x] : 0ull;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) best = max_key(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (threadIdx.x == 0) *token = static_cast<int>(~static_cast<unsigned>(best & 0xffffffffull));
+  }
+}
+
+cudaError_t argmax_launch(const __half* y, int n, int* token, cudaStream_t st) {
+  argmax_kernel<<<1, 1024, 0, st>>>(y, n, token);
+  return cudaGetLastError();
+}
+
+__global__ void argmax_finalize_kernel(unsigned long long* key, int* token) {
+  pdl_launch_dependents();
+  pdl_wait();  // every CTA of the kArgmax grid has folded its key in
+  const unsigned long long k = *reinterpret_cast<volatile unsigned long long*>(key);
+  *token = static_cast<int>(~static_cast<unsigned>(k & 0xffffffffull));
+  *key = 0ull;
+}
+
+cudaError_t argmax_finalize_launch(unsigned long long* key, int* token, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, argmax_finalize_kernel, key, token);
+}
+
 // Self-test of the bounded waits: one thread waits on an mbarrier that no
 // thread ever arrives on, with the given limit; the wait must give up, set
 // the timeout bit and return, leaving the context usable.

@@ -15,6 +15,7 @@ enum Mode : int {
   kSwiglu = 2,   // h = silu(Wg xt) * (Wu xt), xt optionally RMS-normalised
   kMoeUp = 3,    // per active expert: h_k = silu(Wg[e] x) * (Wu[e] x)  -> fp32 workspace
   kMoeDown = 4,  // y = r + sum_k wt_k Wd[e_k] h_k
+  kArgmax = 5,   // y = W x, and the index of its largest element (greedy lm_head)
 };
 
 constexpr int kMaxStages = 16;
@@ -47,6 +48,9 @@ struct StreamArgs {
   int stage_bytes;
   int interleave;           // 1: CTAs take stages round-robin (see StageWalker)
   int prefill;              // stages the producer issues before the activations are in
+  // kArgmax: the 64-bit (value, index) key the CTAs fold their rows into
+  // (zero on entry; argmax_finalize_launch reads it and zeroes it again).
+  unsigned long long* am_key;
   // kPlain: when gather_hd > 0, x is the attention output of a decode over
   // one cached position gathered from qkv (x points at qkv): query head h
   // reads value head h / (gather_nq / gather_nkv) of head_dim gather_hd.
@@ -221,6 +225,13 @@ cudaError_t stream_moe_down(const StreamPlan& p, const StreamArgs& a, cudaStream
                             int device);
 cudaError_t stream_batch(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                          int device);
+cudaError_t stream_argmax(const StreamPlan& p, const StreamArgs& a, cudaStream_t st, int device);
+// Single-CTA argmax of an fp16 vector (the fallback when the streaming kernel
+// does not take the shape): token = lowest index of the largest element.
+cudaError_t argmax_launch(const __half* y, int n, int* token, cudaStream_t st);
+// After a kArgmax launch: once its grid has completed, token = the index in
+// *key, and *key = 0 (programmatic dependent launch: one thread).
+cudaError_t argmax_finalize_launch(unsigned long long* key, int* token, cudaStream_t st);
 cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t st);
 cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t st);
 cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n_kv,

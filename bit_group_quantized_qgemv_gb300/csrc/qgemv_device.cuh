@@ -110,6 +110,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Order-preserving 64-bit key of (fp32 value, index): larger value first,
+// then the lower index; 0 is below every key.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int index) {
+  unsigned b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(b) << 32) | static_cast<unsigned>(~index);
+}
+
+__device__ __forceinline__ unsigned long long max_key(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
 // Programmatic dependent launch: let the next kernel of the stream start
 // launching (its CTAs take SMs as this grid's CTAs exit), and wait until
 // the previous kernel's grid has completed with its memory visible.  Both

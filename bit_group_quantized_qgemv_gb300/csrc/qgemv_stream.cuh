@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
     // squares).  It reads residuals and writes y, so it waits for the
     // previous kernel first.
     pdl_wait();
+    unsigned long long am_best = 0;  // kArgmax: this lane's best (value, index) key
     float rstd = 1.f;
     if (use_gamma) {
       // Slot 0's warps store their sums of x^2 before arriving on xready,
@@ -449,6 +450,10 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
           else if (a.residual != nullptr)
             o += __half2float(a.residual[gr]);
           a.y[gr] = __float2half_rn(o);
+        } else if (MODE == kArgmax) {
+          const __half h = __float2half_rn(v[0]);
+          a.y[gr] = h;
+          am_best = max_key(am_best, argmax_key(__half2float(h), gr));
         } else if (MODE == kNorm) {
           a.y[gr] = __float2half_rn(v[0] * rstd);
         } else if (MODE == kSwiglu) {
@@ -461,6 +466,17 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
       wk.advance(n);
+    }
+    if (MODE == kArgmax) {
+      // The CTA's best (value, index) into the global key with a reduction
+      // that returns nothing, so the CTA does not wait for it; the finalize
+      // kernel that follows reads the key once this grid has completed.
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        am_best = max_key(am_best, __shfl_xor_sync(0xffffffffu, am_best, o));
+      if (lane == 0)
+        asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(a.am_key), "l"(am_best)
+                     : "memory");
     }
     return;
   }

@@ -265,6 +265,30 @@ int qgemv_last_cuda_error(void);
 int qgemv_device_status(unsigned *flags);
 
 /*
+ * qgemv_lm_head_argmax -- greedy decoding of the last matvec of a decode
+ * step (INFERENCE_RESEARCH.md section 1: lm_head and sampling on the GPU,
+ * only the token read back): logits = W . x exactly as qgemv_w4g64 (M = 1),
+ * and *token = the lowest index n of the largest logits[n] (the fp16 values
+ * compared; NaNs are not expected).  codes/scales/biases: 4-bit g64 as
+ * qgemv_w4g64, N rows (the vocabulary), K columns; x fp16 [K]; logits fp16
+ * [N] device output (required); token: device int32.  scratch: device,
+ * 8-byte aligned, qgemv_argmax_scratch_bytes() bytes, zeroed by the caller
+ * before its first use; every call leaves it zero again.  Calls sharing a
+ * scratch must not overlap on the GPU.  When the streaming kernel takes the
+ * shape (K a multiple of 1024, at most 16384, 16-byte-aligned operands) its
+ * epilogue folds each CTA's rows into one 64-bit (value, index) key in the
+ * scratch with a reduction that returns nothing, and a one-thread kernel
+ * chained by programmatic dependent launch turns the key into the index;
+ * otherwise the generic GEMV and a one-CTA argmax kernel.
+ */
+int qgemv_lm_head_argmax(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                         const uint16_t *x, uint16_t *logits, int N, int K, void *scratch,
+                         int32_t *token, void *stream);
+
+/* Bytes of the scratch qgemv_lm_head_argmax needs (16). */
+size_t qgemv_argmax_scratch_bytes(void);
+
+/*
  * qgemv_selftest_wait_timeout -- health check of the bounded device waits
  * every kernel uses: enqueues one tiny kernel on `stream` whose thread waits
  * on a shared-memory mbarrier that nothing ever arrives on, with a limit of

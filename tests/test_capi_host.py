@@ -30,7 +30,8 @@ def test_header_lists_the_boundary():
     for n in ["qgemv_w4g64", "qgemv_w2g64", "rmsnorm_qgemv", "swiglu_qgemv",
               "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
               "decode_attention_seq1", "qgemv_device_status",
-              "qgemv_selftest_wait_timeout", "qgemv_decode_stack"]:
+              "qgemv_selftest_wait_timeout", "qgemv_decode_stack", "qgemv_lm_head_argmax",
+              "qgemv_argmax_scratch_bytes"]:
         assert n in names
 
 
@@ -79,6 +80,20 @@ def test_bad_scalar_status(q):
     assert q.lib.decode_attention_seq1(p, p, 6, 4, 128, None) == -1
     for limit in (0, 1000001):
         assert q.lib.qgemv_selftest_wait_timeout(limit, None) == -1
+    for N, K in ((0, 1024), (8, 96), (8, 0)):
+        assert q.lib.qgemv_lm_head_argmax(p, p, p, p, p, N, K, p, p, None) == -1
+
+
+def test_lm_head_argmax_host_checks(q):
+    p, two, four = _fake_ptr(), _fake_ptr(0x10002), _fake_ptr(0x10004)
+    L = q.lib
+    for i in range(7):
+        args = [p] * 5 + [8, 64] + [p, p]
+        args[[0, 1, 2, 3, 4, 7, 8][i]] = None
+        assert L.qgemv_lm_head_argmax(*args, None) == -2
+    assert L.qgemv_lm_head_argmax(p, p, p, p, p, 8, 64, four, p, None) == -3   # scratch: 8 B
+    assert L.qgemv_lm_head_argmax(p, p, p, p, p, 8, 64, p, two, None) == -3    # token: 4 B
+    assert q.argmax_scratch_bytes() == 16
 
 
 def test_misaligned_status(q):
