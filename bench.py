@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--op", default="stack",
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, lm_head, lm_head_argmax, gemv1024, "
-                        "qwen_stack, w2_layer, m2, m4, m8, m8_w2, or all")
+                        "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
                         "enough to exceed 3x L2; 1 keeps them resident in L2, the "
@@ -470,7 +470,7 @@ def run_own(args):
 
 
 OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "lm_head_argmax", "gemv1024",
-       "qwen_stack", "w2_layer", "m2", "m4", "m8", "m8_w2"]
+       "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2"]
 
 
 def run_op(args):
@@ -574,18 +574,21 @@ def run_one_op(args, name):
             else:
                 q.qgemv_w4g64(w[0], x, y=y)
         launches = 1
-    elif name == "w2_layer":
-        config = "config 4: the five matvecs of one 8B-shaped layer at 2-bit"
-        layer = synth.llama_layer(4, 0, 2)
+    elif name in ("w2_layer", "w8_layer"):
+        wb = 2 if name == "w2_layer" else 8
+        config = ("config 4: the five matvecs of one 8B-shaped layer at 2-bit" if wb == 2 else
+                  "Q8 group 64: the five matvecs of one 8B-shaped layer at 8-bit")
+        layer = synth.llama_layer(4 if wb == 2 else 5, 0, wb)
         shapes = [("qkv", qkv_n, H), ("o", H, H), ("gate", I, H), ("up", I, H), ("down", H, I)]
         base = tuple(up(layer[k]) for k, _, _ in shapes)
-        nbytes = sum(acc.matvec_bytes(n, k, 2) for _, n, k in shapes)
+        nbytes = sum(acc.matvec_bytes(n, k, wb) for _, n, k in shapes)
         xs = {H: torch.randn(H, device=dev).half(), I: torch.randn(I, device=dev).half()}
         y = torch.empty(max(I, qkv_n), device=dev).half()
+        fn = q.qgemv_w2g64 if wb == 2 else q.qgemv_w8g64
 
         def call(w):
             for (key, n, k), wi in zip(shapes, w):
-                q.qgemv_w2g64(wi, xs[k], y=y[:n])
+                fn(wi, xs[k], y=y[:n])
         launches = len(shapes)
     elif name in ("m2", "m4", "m8", "m8_w2"):
         M = int(name[1])

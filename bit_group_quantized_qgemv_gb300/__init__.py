@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     moe_workspace_bytes,
     qgemv_w2g64,
     qgemv_w4g64,
+    qgemv_w8g64,
     rmsnorm_qgemv,
     selftest_wait_timeout,
     strerror,

@@ -22,6 +22,7 @@ _F = ctypes.c_float
 _SIGS = {
     "qgemv_w4g64": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "qgemv_w2g64": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "qgemv_w8g64": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "rmsnorm_qgemv": (_I, [_P, _P, _P, _P, _P, _F, _P, _I, _I, _P]),
     "swiglu_qgemv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _I, _I, _P]),
     "moe_qgemv_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
@@ -162,6 +163,11 @@ def lm_head_argmax(w, x, logits=None, scratch=None, token=None, stream=None):
                                   N, K, _ptr(scratch), _ptr(token), _stream(stream))
     _check(st, "qgemv_lm_head_argmax")
     return token, logits
+
+
+def qgemv_w8g64(w, x, y=None, residual=None, stream=None):
+    """y = W x (+ residual) for an 8-bit g64 weight w = (codes, scales, biases)."""
+    return _plain(lib.qgemv_w8g64, 8, w, x, y, residual, stream)
 
 
 def rmsnorm_qgemv(w, x, norm_weight, eps=1e-5, y=None, stream=None):

@@ -115,6 +115,12 @@ int qgemv_w2g64(const uint32_t* codes, const uint16_t* scales, const uint16_t* b
   return plain_impl(2, codes, scales, biases, x, y, M, N, K, residual, stream);
 }
 
+int qgemv_w8g64(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                const uint16_t* x, uint16_t* y, int M, int N, int K, const uint16_t* residual,
+                void* stream) {
+  return plain_impl(8, codes, scales, biases, x, y, M, N, K, residual, stream);
+}
+
 int rmsnorm_qgemv(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
                   const uint16_t* x, const uint16_t* norm_weight, float eps, uint16_t* y, int N,
                   int K, void* stream) {

@@ -180,7 +180,9 @@ static cudaError_t launch_plain_m(const StreamArgs& a, cudaStream_t st) {
 cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   switch (mode) {
-    case kPlain: return bits == 4 ? launch_plain_m<4>(a, st) : launch_plain_m<2>(a, st);
+    case kPlain:
+      return bits == 4 ? launch_plain_m<4>(a, st)
+                       : (bits == 8 ? launch_plain_m<8>(a, st) : launch_plain_m<2>(a, st));
     case kNorm: return launch_generic_t<4, kNorm, 1>(a, st);
     case kSwiglu: return launch_generic_t<4, kSwiglu, 1>(a, st);
     case kMoeUp: return launch_generic_t<4, kMoeUp, 1>(a, st);

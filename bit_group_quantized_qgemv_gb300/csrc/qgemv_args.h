@@ -94,7 +94,8 @@ inline StreamPlan make_stream_plan(int mode, int bits, int K, long long rows, in
                                    int stage_limit = 40 * 1024, int ring_budget = 200 * 1024,
                                    bool interleave_ok = true) {
   StreamPlan p;
-  if ((bits != 4 && bits != 2) || K % 1024 != 0 || K / kSliceK > 512 || rows <= 0 || sms <= 0)
+  if ((bits != 4 && bits != 2 && bits != 8) || K % 1024 != 0 || K / kSliceK > 512 || rows <= 0 ||
+      sms <= 0)
     return p;
   const int kpt = kSliceK;
   const int tg = K / kpt;

@@ -253,6 +253,31 @@ __device__ __forceinline__ void dot_word2(uint32_t w, const uint32_t* xp, float&
         "r"(xp[6]), "r"(xp[7]));
 }
 
+// An 8-bit word holds codes q_0..q_3 (k = 4i .. 4i+3), low byte first.
+// Masking with 0x00FF00FF keeps q_0 and q_2 as fp16 subnormals q * 2^-24
+// (exact: q < 1024), and the word shifted right by 8 gives q_1 and q_3 the
+// same way, so one accumulator takes all four products: a += q x 2^-24.
+// Activations packed xp[0] = (x_{4i}, x_{4i+2}), xp[1] = (x_{4i+1}, x_{4i+3}).
+__device__ __forceinline__ void dot_word8(uint32_t w, const uint32_t* xp, float& a, float& b) {
+  asm("{\n"
+      ".reg .b32 v0, v1;\n"
+      ".reg .b16 q0, q1, q2, q3, x0, x1, x2, x3;\n"
+      "and.b32 v0, %2, 0x00FF00FF;\n"
+      "shr.u32 v1, %2, 8;\n"
+      "and.b32 v1, v1, 0x00FF00FF;\n"
+      "mov.b32 {q0, q2}, v0;\n"
+      "mov.b32 {q1, q3}, v1;\n"
+      "mov.b32 {x0, x2}, %3;\n"
+      "mov.b32 {x1, x3}, %4;\n"
+      "fma.rn.f32.f16 %0, q0, x0, %0;\n"
+      "fma.rn.f32.f16 %1, q1, x1, %1;\n"
+      "fma.rn.f32.f16 %0, q2, x2, %0;\n"
+      "fma.rn.f32.f16 %1, q3, x3, %1;\n"
+      "}"
+      : "+f"(a), "+f"(b)
+      : "r"(w), "r"(xp[0]), "r"(xp[1]));
+}
+
 // Code q of k within a packed word (generic path).
 template <int BITS>
 __device__ __forceinline__ int unpack_code(uint32_t word, int j) {

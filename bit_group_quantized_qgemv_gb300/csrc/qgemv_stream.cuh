@@ -159,6 +159,17 @@ __device__ __forceinline__ float task_dot(const uint8_t* codes, const uint32_t* 
       dot_word4(c.w, xp + 16 * q + 12, a1, b1);
     }
     t = fmaf(b0 + b1, 0.0625f, a0 + a1);
+  } else if (BITS == 8) {
+    float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < KPT / 16; ++q) {
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + 16 * q);
+      dot_word8(c.x, xp + 8 * q + 0, a0, b0);
+      dot_word8(c.y, xp + 8 * q + 2, a1, b1);
+      dot_word8(c.z, xp + 8 * q + 4, a0, b0);
+      dot_word8(c.w, xp + 8 * q + 6, a1, b1);
+    }
+    t = (a0 + b0) + (a1 + b1);
   } else {
     float ca = 0.f, cb = 0.f, cc = 0.f, cd = 0.f;
 #pragma unroll
@@ -242,6 +253,14 @@ __device__ __forceinline__ void load_task_x(const __half* x, const __half* gamma
         for (int j = 0; j < 4; ++j)
           xp[8 * c + 4 * i + j] = static_cast<uint32_t>(hv[8 * i + j]) |
                                   (static_cast<uint32_t>(hv[8 * i + j + 4]) << 16);
+    } else if (BITS == 8) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // word i of the chunk: k = 4i .. 4i+3
+        xp[8 * c + 2 * i] =
+            static_cast<uint32_t>(hv[4 * i]) | (static_cast<uint32_t>(hv[4 * i + 2]) << 16);
+        xp[8 * c + 2 * i + 1] =
+            static_cast<uint32_t>(hv[4 * i + 1]) | (static_cast<uint32_t>(hv[4 * i + 3]) << 16);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j)

@@ -1,4 +1,4 @@
-// Streaming kernels: plain 4-bit and 2-bit GEMV (optionally + residual), and
+// Streaming kernels: plain 4-, 8- and 2-bit GEMV (optionally + residual), and
 // the 4-bit GEMV with the index of its largest output (greedy lm_head).
 #include "qgemv_stream.cuh"
 
@@ -7,6 +7,7 @@ namespace qgemv {
 cudaError_t stream_plain(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                          int device) {
   if (bits == 4) return launch_stream<4, kPlain>(p, a, st, device);
+  if (bits == 8) return launch_stream<8, kPlain>(p, a, st, device);
   return launch_stream<2, kPlain>(p, a, st, device);
 }
 

@@ -83,6 +83,18 @@ int qgemv_w2g64(const uint32_t *codes, const uint16_t *scales, const uint16_t *b
                 const uint16_t *residual, void *stream);
 
 /*
+ * qgemv_w8g64 -- the same product with 8-bit codes (Q8 group 64, the other
+ * quantisation level the BaseRT page, "BaseRT: Best-in-Class LLM Inference
+ * on Apple Silicon via Native Metal", evaluates beside Q4, in the planar
+ * layout of INFERENCE_RESEARCH.md section 3 item 4): codes [N][K/4] uint32,
+ * 4 codes per word, low byte first; w = q * scale + bias with q in 0..255.
+ * Other arguments and checks as qgemv_w4g64 (M > 1 takes the generic kernel).
+ */
+int qgemv_w8g64(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                const uint16_t *x, uint16_t *y, int M, int N, int K,
+                const uint16_t *residual, void *stream);
+
+/*
  * rmsnorm_qgemv -- y = W . (x * gamma / sqrt(mean(x^2) + eps)), M = 1,
  * 4-bit g64.  The RMSNorm + QKV matvec fusion of INFERENCE_RESEARCH.md
  * section 1 (and the RMS normalisation shader on the hada.io page).

@@ -16,6 +16,10 @@
  *     group 64).  2-bit codes (16 per uint32, low bits first) follow the
  *     same layout; the 2-bit experts are on the hada.io news page
  *     (topic 27758), "Resultats de performance" and "Shaders de calcul Metal".
+ *     8-bit codes (4 per uint32, low byte first) likewise: Q8, the level the
+ *     BaseRT page ("BaseRT: Best-in-Class LLM Inference on Apple Silicon via
+ *     Native Metal") evaluates beside Q4.  oracle_code() reads any of the
+ *     three widths (32 / bits codes per word).
  *   - Dequantisation w = q*scale + bias and its product with x: the hada.io
  *     page, "Noyau de dequantification optimise FMA" ((nibble*scale+bias)*x,
  *     rewritten as fma(nibble, scale*x, bias*x); an exact identity, so the

@@ -14,6 +14,10 @@ Tensor ids (the third seed word):
     5 down                    6 lm_head          7 MoE gate.up  8 MoE down
     10 x (activation)         11 residual        12 norm gamma (first norm)
     13 norm gamma (second)    14 MoE routing     15 spare weight
+
+Workloads (the first seed word): 0 the 1024 x 1024 GEMV, 1 the
+Llama-3.1-8B-shaped layer, 2 the Qwen3-0.6B-shaped stack, 3 the MoE, 4 the
+2-bit layer and small batches, 5 the 8-bit (Q8) layer.
 """
 from __future__ import annotations
 
@@ -63,9 +67,12 @@ def quant_weight(g: np.random.Generator, N: int, K: int, bits: int = 4,
     bias = fp16(-8 * scale + N(0, 0.001)) per (row, group).
     2-bit: codes uniform 0..3; scale ~ U(0.02, 0.08) rounded to fp16;
     bias = fp16(-1.5 * scale), no noise.
+    8-bit: codes uniform 0..255; scale ~ U(0.0003125, 0.00125) (the 4-bit
+    range / 16, so weights span the same range) rounded to fp16;
+    bias = fp16(-128 * scale + N(0, 0.001)).
     ``lead`` prepends leading dimensions (e.g. (E,) for expert stacks).
     """
-    assert bits in (2, 4) and K % 64 == 0
+    assert bits in (2, 4, 8) and K % 64 == 0
     words = K * bits // 32
     G = K // 64
     codes = g.integers(0, 0xFFFFFFFF, size=lead + (N, words), dtype=np.uint32,
@@ -74,6 +81,10 @@ def quant_weight(g: np.random.Generator, N: int, K: int, bits: int = 4,
         s = g.uniform(0.005, 0.02, size=lead + (N, G)).astype(np.float16)
         noise = g.normal(0.0, 0.001, size=lead + (N, G))
         b = (-8.0 * s.astype(np.float64) + noise).astype(np.float16)
+    elif bits == 8:
+        s = g.uniform(0.0003125, 0.00125, size=lead + (N, G)).astype(np.float16)
+        noise = g.normal(0.0, 0.001, size=lead + (N, G))
+        b = (-128.0 * s.astype(np.float64) + noise).astype(np.float16)
     else:
         s = g.uniform(0.02, 0.08, size=lead + (N, G)).astype(np.float16)
         b = (-1.5 * s.astype(np.float64)).astype(np.float16)
@@ -117,7 +128,7 @@ MOE = dict(hidden=4096, inter=1024, n_experts=512, top_k=4, tokens=16)
 
 
 def llama_layer(workload: int, layer: int, bits: int = 4) -> dict:
-    """Weights and inputs of one Llama-8B-shaped layer (4-bit unless bits=2)."""
+    """Weights and inputs of one Llama-8B-shaped layer (bits 4, 2 or 8)."""
     c = LLAMA8B
     H, I = c["hidden"], c["inter"]
     qkv_n = (c["n_q"] + 2 * c["n_kv"]) * c["head_dim"]

@@ -64,6 +64,7 @@ def test_bad_shape_status(q, M, N, K):
     p = _fake_ptr()
     assert q.lib.qgemv_w4g64(p, p, p, p, p, M, N, K, None, None) == -1
     assert q.lib.qgemv_w2g64(p, p, p, p, p, M, N, K, None, None) == -1
+    assert q.lib.qgemv_w8g64(p, p, p, p, p, M, N, K, None, None) == -1
 
 
 def test_bad_scalar_status(q):

@@ -175,3 +175,16 @@ def test_config4_two_bit_layer_shapes():
         y = q.qgemv_w2g64(dev_weight(w), dev16(x))
         y64, _, bound = oracle.qgemv(2, w.codes, w.scales, w.biases, x)
         check(y, y64, plain_tol(bound), f"config 4 w2 {name}")
+
+
+def test_q8_layer_shapes():
+    """8-bit (Q8 group 64) at the Llama-3.1-8B layer's matvec shapes, in the
+    streaming launch the benchmark's w8_layer unit times."""
+    shapes = {"qkv": (6144, 4096), "o": (4096, 4096), "gate": (14336, 4096),
+              "down": (4096, 14336)}
+    for name, (N, K) in shapes.items():
+        w = synth.quant_weight(synth.rng(5, 0, synth.TID[name]), N, K, 8)
+        x = synth.activation(synth.rng(5, 1, synth.TID["x"], K), K)
+        y = q.qgemv_w8g64(dev_weight(w), dev16(x))
+        y64, _, bound = oracle.qgemv(8, w.codes, w.scales, w.biases, x)
+        check(y, y64, plain_tol(bound), f"q8 {name}")

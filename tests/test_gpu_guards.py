@@ -60,6 +60,8 @@ def X(seed, K, M=None):
     (4, 601, 4096, 3),     # small-batch kernel
     (4, 100, 2048, 8),
     (2, 203, 14336, 8),    # small-batch, two passes of 4 rows
+    (8, 1000, 2048, 1),    # 8-bit streaming
+    (8, 203, 4096, 3),     # 8-bit, M > 1 (generic kernel)
 ])
 def test_plain_writes_only_y(bits, N, K, M):
     w = W(N + K + M, N, K, bits)
@@ -67,7 +69,7 @@ def test_plain_writes_only_y(bits, N, K, M):
     r = X(N + 7, N, None if M == 1 else M)
     buf, y = guarded(M * N)
     y = y.view(N) if M == 1 else y.view(M, N)
-    fn = q.qgemv_w4g64 if bits == 4 else q.qgemv_w2g64
+    fn = {4: q.qgemv_w4g64, 2: q.qgemv_w2g64, 8: q.qgemv_w8g64}[bits]
     fn(dev_weight(w), dev16(x), y=y, residual=dev16(r))
     torch.cuda.synchronize()
     assert_guards(buf, M * N, f"w{bits} N={N} K={K} M={M}")

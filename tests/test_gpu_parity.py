@@ -28,7 +28,7 @@ def X(seed, K, M=None):
 
 
 def run_plain(bits, w, x, residual=None, y=None):
-    fn = q.qgemv_w4g64 if bits == 4 else q.qgemv_w2g64
+    fn = {4: q.qgemv_w4g64, 2: q.qgemv_w2g64, 8: q.qgemv_w8g64}[bits]
     return fn(dev_weight(w), x if torch.is_tensor(x) else dev16(x),
               y=y, residual=None if residual is None else
               (residual if torch.is_tensor(residual) else dev16(residual)))
@@ -45,6 +45,19 @@ def test_hand_example_a_exact():
                               np.full((1, reps), float(d["biases"]), np.float16), 4)
         xx = np.concatenate([x, np.zeros(64 * (reps - 1), np.float16)])
         y = run_plain(4, w, xx)
+        assert float(y[0]) == float(d["y"])
+
+
+def test_hand_example_c_8bit_exact():
+    d = load_golden("hand_example_c.txt")
+    words = np.array([int(v, 16) for v in d["words"].split()], np.uint32)
+    x = np.array([float(v) for v in d["x"].split()], np.float16)
+    for reps in (1, 16):          # K = 64 (generic kernel) and K = 1024 (streaming)
+        w = synth.QuantWeight(np.tile(words, reps)[None, :],
+                              np.full((1, reps), float(d["scales"]), np.float16),
+                              np.full((1, reps), float(d["biases"]), np.float16), 8)
+        xx = np.concatenate([x, np.zeros(64 * (reps - 1), np.float16)])
+        y = run_plain(8, w, xx)
         assert float(y[0]) == float(d["y"])
 
 
@@ -66,9 +79,13 @@ FAST = [(4, 1024, 1024), (4, 7, 1024), (4, 1000, 2048), (4, 333, 3072), (4, 4099
         (4, 152, 1024), (4, 153, 2048)]
 GENERIC = [(4, 5, 64), (4, 17, 192), (4, 33, 960), (4, 3, 1088), (2, 9, 128), (2, 40, 1024),
            (2, 11, 3072)]
+# 8-bit (Q8 group 64): streaming shapes (ragged bands, K up to 14336) and
+# shapes the generic kernel takes
+EIGHT = [(8, 1000, 2048), (8, 4099, 4096), (8, 601, 14336), (8, 7, 1024), (8, 153, 2048),
+         (8, 5, 64), (8, 33, 960), (8, 3, 1088)]
 
 
-@pytest.mark.parametrize("bits,N,K", FAST + GENERIC)
+@pytest.mark.parametrize("bits,N,K", FAST + GENERIC + EIGHT)
 @pytest.mark.parametrize("with_res", [False, True])
 def test_plain_parity(bits, N, K, with_res):
     w = W(N * 7 + K + bits, N, K, bits)
@@ -79,7 +96,7 @@ def test_plain_parity(bits, N, K, with_res):
     check(y, y64, plain_tol(bound), f"w{bits} N={N} K={K} res={with_res}")
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 @pytest.mark.parametrize("M", [2, 3, 8])
 def test_small_batch(bits, M):
     N, K = 203, 2048

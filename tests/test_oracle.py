@@ -24,7 +24,9 @@ def np_unpack(codes, bits):
     """Unpack packed rows through a little-endian byte view (independent of
     the oracle's word/shift arithmetic).  Returns int64 [..., K]."""
     b = np.ascontiguousarray(codes).view(np.uint8)
-    if bits == 4:
+    if bits == 8:
+        parts = [b]
+    elif bits == 4:
         parts = [b & 0xF, b >> 4]
     else:
         parts = [(b >> s) & 0x3 for s in (0, 2, 4, 6)]
@@ -73,7 +75,7 @@ def test_double_to_half_matches_numpy_rne():
 
 
 # ----------------------------------------------------------------- unpack
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_unpack_against_byte_view(bits):
     g = np.random.default_rng(bits)
     row = g.integers(0, 2**32, size=8, dtype=np.uint64).astype(np.uint32)
@@ -98,6 +100,22 @@ def test_hand_example_a():
     q_hi = np.array([7 - k for k in range(8)] + [0] * 56)
     xv = x.astype(np.float64)
     assert np.sum((0.5 * q_hi - 4) * xv * (np.arange(64) < 8)) == float(d["y_high_nibble_first"])
+
+
+def test_hand_example_c_8bit():
+    d = load_golden("hand_example_c.txt")
+    words = np.array([int(w, 16) for w in d["words"].split()], np.uint32)[None, :]
+    s = np.array([[float(d["scales"])]], np.float16)
+    b = np.array([[float(d["biases"])]], np.float16)
+    x = np.array([float(v) for v in d["x"].split()], np.float16)
+    y64, y16, _ = oracle.qgemv(8, words, s, b, x)
+    assert y64[0] == float(d["y"])
+    assert float(y16[0]) == float(d["y"])
+    # the fixture's misread value really is what the other byte order gives
+    assert float(d["y_high_byte_first"]) != float(d["y"])
+    q_hi = np.array([3, 2, 1, 0, 7, 6, 5, 4] + [0] * 56)
+    xv = x.astype(np.float64)
+    assert np.sum((0.5 * q_hi - 16) * xv * (np.arange(64) < 8)) == float(d["y_high_byte_first"])
 
 
 def test_hand_example_b():
@@ -148,8 +166,24 @@ def test_unit_scale_zero_bias_is_integer_dot(bits, K):
     assert np.array_equal(y16.astype(np.float64), ref.astype(np.float64))
 
 
+def test_unit_scale_zero_bias_is_integer_dot_8bit():
+    # eight nonzero activations in {-1, 1}: |y| <= 8 * 255 = 2040, exact in fp16
+    K = 128
+    g = np.random.default_rng(8)
+    w = small_weight(2, 5, K, 8)
+    w.scales[:] = 1.0
+    w.biases[:] = 0.0
+    x = np.zeros(K, np.float16)
+    x[g.choice(K, size=8, replace=False)] = g.choice([-1.0, 1.0], size=8)
+    y64, y16, _ = oracle.qgemv(8, w.codes, w.scales, w.biases, x)
+    q = np_unpack(w.codes, 8)
+    ref = q @ x.astype(np.int64)
+    assert np.array_equal(y64, ref.astype(np.float64))
+    assert np.array_equal(y16.astype(np.float64), ref.astype(np.float64))
+
+
 # -------------------------------------------------------- brute force
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("N,K,M", [(1, 64, 1), (3, 192, 2), (17, 320, 3), (64, 512, 8)])
 def test_brute_force_dense(bits, N, K, M):
     w = small_weight(N * 1000 + K, N, K, bits)
@@ -166,6 +200,22 @@ def test_brute_force_dense(bits, N, K, M):
         assert np.allclose(y64, ref, rtol=1e-12, atol=1e-12 * mag.max())
         assert np.allclose(bound, mag, rtol=1e-12)
         assert np.array_equal(y16, y64.astype(np.float16))
+
+
+def test_four_bit_reencoded_as_eight_bit():
+    K, N = 256, 7
+    w4 = small_weight(5, N, K, 4)
+    q = np_unpack(w4.codes, 4)                       # values 0..15
+    # repack the same codes 4 per word, one per byte, low byte first
+    q4 = q.reshape(N, K // 4, 4).astype(np.uint64)
+    words8 = np.zeros((N, K // 4), np.uint64)
+    for j in range(4):
+        words8 |= q4[:, :, j] << np.uint64(8 * j)
+    words8 = words8.astype(np.uint32)
+    x = synth.activation(synth.rng(100, 5, 10), K)
+    y4, _, _ = oracle.qgemv(4, w4.codes, w4.scales, w4.biases, x)
+    y8, _, _ = oracle.qgemv(8, words8, w4.scales, w4.biases, x)
+    assert np.array_equal(y4, y8)
 
 
 def test_two_bit_reencoded_as_four_bit():
