@@ -224,3 +224,30 @@ def moe_qgemv_combine(gu, dn, idx, wt, x, residual):
                                    _ptr(y64), _ptr(y16), _ptr(tol),
                                    ctypes.addressof(err))
     return y64, y16.view(np.float16), tol, int(err.value)
+
+
+def moe_route(logits, top_k: int, shared: int = 0):
+    """MoE routing of one token from its router logits (the hada.io page,
+    topic 27758, "Architecture du modele": K = 4 active experts of 512, one
+    of them shared; which experts and with what weights is the reading the
+    tests use): the shared expert (when ``shared`` >= 0), then the routed
+    experts with the largest logits, one at a time, the lower index winning
+    a tie, until ``top_k`` are chosen; the weights are the softmax of the
+    chosen logits, in fp64.  ``logits``: fp16 [E] (the selection is decided
+    on these values).  Returns (idx int32 [top_k] in choice order, weights
+    float64 [top_k])."""
+    lv = [float(v) for v in np.asarray(logits, np.float16).astype(np.float64)]
+    chosen = [int(shared)] if shared >= 0 else []
+    while len(chosen) < top_k:
+        best = -1
+        for e in range(len(lv)):
+            if e in chosen:
+                continue
+            if best < 0 or lv[e] > lv[best]:  # strict: the lower index keeps a tie
+                best = e
+        chosen.append(best)
+    sel = [lv[e] for e in chosen]
+    m = max(sel)
+    ex = [float(np.exp(v - m)) for v in sel]
+    tot = sum(ex)
+    return np.array(chosen, np.int32), np.array([v / tot for v in ex], np.float64)

@@ -390,3 +390,39 @@ def test_moe_duplicate_index_counts_twice():
     y1, _, _, _ = _call_moe(gu, dn, np.array([1], np.int32),
                             np.array([0.5], np.float32), x, zero)
     assert np.allclose(y2, y1, rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------- MoE routing
+def test_moe_route_hand_example():
+    # E = 6, shared expert 0, top_k = 4: routed = 3 (3.0), then 1 and 5 tie
+    # at 2.0 and the lower index comes first
+    logits = np.array([0.5, 2.0, 1.0, 3.0, -1.0, 2.0], np.float16)
+    idx, wt = oracle.moe_route(logits, 4, 0)
+    assert idx.tolist() == [0, 3, 1, 5]
+    e = np.exp(np.array([0.5, 3.0, 2.0, 2.0]))
+    assert np.allclose(wt, e / e.sum(), rtol=1e-15)
+
+
+def test_moe_route_equal_logits_and_no_shared_expert():
+    idx, wt = oracle.moe_route(np.zeros(10, np.float16), 4, 0)
+    assert idx.tolist() == [0, 1, 2, 3] and np.allclose(wt, 0.25, rtol=1e-15)
+    idx, wt = oracle.moe_route(np.zeros(10, np.float16), 3, -1)
+    assert idx.tolist() == [0, 1, 2] and np.allclose(wt, 1 / 3, rtol=1e-15)
+
+
+@pytest.mark.parametrize("E,top_k,shared", [(512, 4, 0), (64, 8, -1), (33, 1, 5), (16, 2, 15)])
+def test_moe_route_against_stable_sort(E, top_k, shared):
+    g = np.random.default_rng(E + top_k)
+    logits = g.normal(0, 1, E).astype(np.float16)
+    logits[g.choice(E, size=E // 4)] = logits[0]          # plenty of exact ties
+    idx, wt = oracle.moe_route(logits, top_k, shared)
+    # independent selection: a stable sort on the negated logits keeps the
+    # lower index first among equal values
+    order = [e for e in np.argsort(-logits.astype(np.float64), kind="stable") if e != shared]
+    want = ([shared] if shared >= 0 else []) + order[:top_k - (1 if shared >= 0 else 0)]
+    assert idx.tolist() == [int(v) for v in want]
+    sel = logits.astype(np.float64)[want]
+    assert abs(wt.sum() - 1.0) < 1e-15
+    # the softmax of the chosen logits, ranked like them
+    assert np.allclose(wt, np.exp(sel - sel.max()) / np.exp(sel - sel.max()).sum(), rtol=1e-14)
+    assert np.all(np.diff(wt[1 if shared >= 0 else 0:]) <= 1e-15)
