@@ -60,7 +60,8 @@ def parse_args():
                    help="skip the single-op CUDA-graph comparison")
     p.add_argument("--op", default="stack",
                    help="time one op or configuration unit alone instead of the stack: "
-                        "qkv, o_proj, swiglu, down, moe, lm_head, lm_head_argmax, gemv1024, "
+                        "qkv, o_proj, swiglu, down, moe, moe_routed, lm_head, lm_head_argmax, "
+                        "gemv1024, "
                         "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
@@ -469,7 +470,8 @@ def run_own(args):
     return 0
 
 
-OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "lm_head", "lm_head_argmax", "gemv1024",
+OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "moe_routed", "lm_head", "lm_head_argmax",
+       "gemv1024",
        "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2"]
 
 
@@ -535,7 +537,7 @@ def run_one_op(args, name):
             else:
                 q.qgemv_w4g64(w[0], xi, y=y[:H], residual=x)
         launches = 1
-    elif name == "moe":
+    elif name in ("moe", "moe_routed"):
         config = "config 3: MoE token, 4 of 512 experts, combine + residual"
         gu, dn = synth.moe_experts(3, 0, 8)
         base = (up(gu), up(dn))
@@ -545,10 +547,22 @@ def run_one_op(args, name):
         wt = torch.tensor([0.4, 0.3, 0.2, 0.1], dtype=torch.float32, device=dev)
         work = torch.empty(4 * 1024, dtype=torch.float32, device=dev)
         y = torch.empty(H, device=dev).half()
+        launches = 2
+        if name == "moe_routed":
+            # the router on the GPU too: an 8 x 4096 router (the 8 resident
+            # experts of the rotated copies), shared expert 0 + 3 routed
+            config = ("config 3: MoE token with its routing on the GPU (router GEMV, top-K "
+                      "selection, softmax) + 4 experts + combine + residual")
+            wr = synth.quant_weight(synth.rng(3, 0, synth.TID["router"]), 8, H, 4)
+            base = (up(gu), up(dn), up(wr))
+            nbytes += acc.matvec_bytes(8, H, 4) + 4 * (4 + 4)
+            rlog = torch.empty(8, device=dev).half()
+            launches = 4
 
         def call(w):
+            if name == "moe_routed":
+                q.moe_router(w[2], x, top_k=4, shared=0, logits=rlog, idx=idx, wt=wt)
             q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y, workspace=work)
-        launches = 2
     elif name in ("lm_head", "lm_head_argmax", "gemv1024"):
         if name == "lm_head":
             config = "config 2: Qwen3-0.6B-shaped lm_head 1024->151936"

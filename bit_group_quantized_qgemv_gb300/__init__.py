@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     lm_head_argmax,
     argmax_scratch_bytes,
     moe_qgemv_combine,
+    moe_router,
     moe_qgemv_combine_noalloc,
     noalloc_max_scratch_bytes,
     moe_workspace_bytes,

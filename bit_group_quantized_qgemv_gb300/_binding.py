@@ -41,6 +41,7 @@ _SIGS = {
     "qgemv_selftest_wait_timeout": (_I, [ctypes.c_uint, ctypes.c_void_p]),
     "qgemv_lm_head_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "qgemv_argmax_scratch_bytes": (ctypes.c_size_t, []),
+    "qgemv_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
 
 #: Names the C header declares (the binding exposes each one).
@@ -135,6 +136,29 @@ def qgemv_w4g64(w, x, y=None, residual=None, stream=None):
 def qgemv_w2g64(w, x, y=None, residual=None, stream=None):
     """y = W x (+ residual) for a 2-bit g64 weight w = (codes, scales, biases)."""
     return _plain(lib.qgemv_w2g64, 2, w, x, y, residual, stream)
+
+
+def moe_router(w, x, top_k=4, shared=0, logits=None, idx=None, wt=None, stream=None):
+    """MoE routing on the GPU (qgemv_moe_router): logits = Wr x (4-bit g64),
+    idx = shared expert + top routed experts, wt = softmax of their logits.
+    Returns (idx int32 [top_k], wt float32 [top_k], logits fp16 [E])."""
+    codes, scales, biases = _weight(w, "w")
+    x = _cuda(x, _F16, "x")
+    E = codes.shape[-2]
+    H = codes.shape[-1] * 8
+    if logits is None:
+        logits = torch.empty(E, dtype=torch.float16, device=x.device)
+    if idx is None:
+        idx = torch.empty(top_k, dtype=torch.int32, device=x.device)
+    if wt is None:
+        wt = torch.empty(top_k, dtype=torch.float32, device=x.device)
+    _cuda(logits, _F16, "logits")
+    _cuda(idx, (torch.int32,), "idx")
+    _cuda(wt, (torch.float32,), "wt")
+    st = lib.qgemv_moe_router(_ptr(codes), _ptr(scales), _ptr(biases), _ptr(x), E, H, int(top_k),
+                              int(shared), _ptr(logits), _ptr(idx), _ptr(wt), _stream(stream))
+    _check(st, "qgemv_moe_router")
+    return idx, wt, logits
 
 
 def argmax_scratch_bytes() -> int:

@@ -306,6 +306,22 @@ int qgemv_device_status(unsigned* flags) {
   return QGEMV_OK;
 }
 
+int qgemv_moe_router(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                     const uint16_t* x, int E, int H, int top_k, int shared_expert,
+                     uint16_t* logits, int32_t* expert_idx, float* expert_w, void* stream) {
+  if (!codes || !scales || !biases || !x || !logits || !expert_idx || !expert_w)
+    return QGEMV_ENULL;
+  if (E < 1 || top_k < 1 || top_k > qgemv::kMaxTopK || top_k > E || shared_expert < -1 ||
+      shared_expert >= E || !valid_k(H))
+    return QGEMV_EINVAL;
+  if (!aligned(expert_idx, 4) || !aligned(expert_w, 4)) return QGEMV_EALIGN;
+  const int rc = plain_impl(4, codes, scales, biases, x, logits, 1, E, H, nullptr, stream);
+  if (rc != QGEMV_OK) return rc;
+  return finish(qgemv::moe_route_launch(reinterpret_cast<const __half*>(logits), E, top_k,
+                                        shared_expert, expert_idx, expert_w,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t qgemv_argmax_scratch_bytes(void) { return 16; }
 
 int qgemv_lm_head_argmax(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,

@@ -271,6 +271,78 @@ cudaError_t argmax_finalize_launch(unsigned long long* key, int* token, cudaStre
   return cudaLaunchKernelEx(&cfg, argmax_finalize_kernel, key, token);
 }
 
+// MoE routing from fp16 router logits, one CTA of 1024 threads: the shared
+// expert (shared >= 0), then the routed experts with the largest logits one
+// at a time (the (value, index) key of argmax_key: the lower index wins a
+// tie), then the softmax of the chosen logits in fp32.
+__global__ void __launch_bounds__(1024) moe_route_kernel(const __half* __restrict__ logits, int E,
+                                                         int top_k, int shared,
+                                                         int* __restrict__ idx,
+                                                         float* __restrict__ wt) {
+  __shared__ unsigned long long s_red[32];
+  __shared__ int s_chosen[kMaxTopK];
+  pdl_launch_dependents();
+  pdl_wait();  // the logits come from the previous kernel
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int n = 0;
+  if (shared >= 0) {
+    if (threadIdx.x == 0) s_chosen[0] = shared;
+    n = 1;
+  }
+  __syncthreads();
+  for (; n < top_k; ++n) {
+    unsigned long long best = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      bool taken = false;
+      for (int j = 0; j < n; ++j) taken = taken || (s_chosen[j] == e);
+      if (!taken) best = max_key(best, argmax_key(__half2float(logits[e]), e));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) best = max_key(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if (lane == 0) s_red[warp] = best;
+    __syncthreads();
+    if (warp == 0) {
+      best = lane < static_cast<int>(blockDim.x >> 5) ? s_red[lane] : 0ull;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1)
+        best = max_key(best, __shfl_xor_sync(0xffffffffu, best, o));
+      if (lane == 0) s_chosen[n] = static_cast<int>(~static_cast<unsigned>(best & 0xffffffffull));
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    float v[kMaxTopK];
+    float m = -INFINITY;
+    for (int j = 0; j < top_k; ++j) {
+      v[j] = __half2float(logits[s_chosen[j]]);
+      m = fmaxf(m, v[j]);
+    }
+    float sum = 0.f;
+    for (int j = 0; j < top_k; ++j) {
+      v[j] = expf(v[j] - m);
+      sum += v[j];
+    }
+    for (int j = 0; j < top_k; ++j) {
+      idx[j] = s_chosen[j];
+      wt[j] = v[j] / sum;
+    }
+  }
+}
+
+cudaError_t moe_route_launch(const __half* logits, int E, int top_k, int shared, int* idx,
+                             float* wt, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_route_kernel, logits, E, top_k, shared, idx, wt);
+}
+
 // Self-test of the bounded waits: one thread waits on an mbarrier that no
 // thread ever arrives on, with the given limit; the wait must give up, set
 // the timeout bit and return, leaving the context usable.

@@ -230,6 +230,11 @@ cudaError_t stream_argmax(const StreamPlan& p, const StreamArgs& a, cudaStream_t
 // Single-CTA argmax of an fp16 vector (the fallback when the streaming kernel
 // does not take the shape): token = lowest index of the largest element.
 cudaError_t argmax_launch(const __half* y, int n, int* token, cudaStream_t st);
+// MoE routing from fp16 logits [E] (one CTA, chained after the router
+// GEMV): idx [top_k] = the shared expert (shared >= 0) and the routed
+// experts with the largest logits, wt [top_k] = their softmax.
+cudaError_t moe_route_launch(const __half* logits, int E, int top_k, int shared, int* idx,
+                             float* wt, cudaStream_t st);
 // After a kArgmax launch: once its grid has completed, token = the index in
 // *key, and *key = 0 (programmatic dependent launch: one thread).
 cudaError_t argmax_finalize_launch(unsigned long long* key, int* token, cudaStream_t st);

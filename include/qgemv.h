@@ -277,6 +277,25 @@ int qgemv_last_cuda_error(void);
 int qgemv_device_status(unsigned *flags);
 
 /*
+ * qgemv_moe_router -- MoE routing of one token on the GPU (the hada.io page,
+ * topic 27758, "Architecture du modele": K active experts of E, one shared;
+ * INFERENCE_RESEARCH.md section 1: keep the routing on the device):
+ * logits = Wr . x (4-bit g64 router weight [E][H], as qgemv_w4g64), then
+ * expert_idx = the shared expert (shared_expert >= 0; -1 for none) followed
+ * by the routed experts with the largest logits, in decreasing order, the
+ * lower index winning a tie (the fp16 logits are compared), until top_k are
+ * chosen; expert_w = softmax of the chosen logits (fp32).  expert_idx int32
+ * [top_k] and expert_w fp32 [top_k] on the device are what
+ * moe_qgemv_combine takes.  logits: fp16 [E] device output (required).
+ * Checks: E >= 1, 1 <= top_k <= 8, top_k <= E, -1 <= shared_expert < E,
+ * H >= 64 and H % 64 == 0.  Two launches (the GEMV, then a one-CTA
+ * selection chained by programmatic dependent launch).
+ */
+int qgemv_moe_router(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                     const uint16_t *x, int E, int H, int top_k, int shared_expert,
+                     uint16_t *logits, int32_t *expert_idx, float *expert_w, void *stream);
+
+/*
  * qgemv_lm_head_argmax -- greedy decoding of the last matvec of a decode
  * step (INFERENCE_RESEARCH.md section 1: lm_head and sampling on the GPU,
  * only the token read back): logits = W . x exactly as qgemv_w4g64 (M = 1),

@@ -14,6 +14,7 @@ Tensor ids (the third seed word):
     5 down                    6 lm_head          7 MoE gate.up  8 MoE down
     10 x (activation)         11 residual        12 norm gamma (first norm)
     13 norm gamma (second)    14 MoE routing     15 spare weight
+    16 MoE router weight
 
 Workloads (the first seed word): 0 the 1024 x 1024 GEMV, 1 the
 Llama-3.1-8B-shaped layer, 2 the Qwen3-0.6B-shaped stack, 3 the MoE, 4 the
@@ -28,7 +29,7 @@ import numpy as np
 TID = {
     "qkv": 1, "o": 2, "gate": 3, "up": 4, "down": 5, "lm_head": 6,
     "moe_gu": 7, "moe_down": 8, "x": 10, "residual": 11, "gamma1": 12,
-    "gamma2": 13, "routing": 14, "spare": 15,
+    "gamma2": 13, "routing": 14, "spare": 15, "router": 16,
 }
 
 

@@ -31,7 +31,7 @@ def test_header_lists_the_boundary():
               "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
               "decode_attention_seq1", "qgemv_device_status",
               "qgemv_selftest_wait_timeout", "qgemv_decode_stack", "qgemv_lm_head_argmax",
-              "qgemv_argmax_scratch_bytes"]:
+              "qgemv_argmax_scratch_bytes", "qgemv_moe_router"]:
         assert n in names
 
 
@@ -83,6 +83,20 @@ def test_bad_scalar_status(q):
         assert q.lib.qgemv_selftest_wait_timeout(limit, None) == -1
     for N, K in ((0, 1024), (8, 96), (8, 0)):
         assert q.lib.qgemv_lm_head_argmax(p, p, p, p, p, N, K, p, p, None) == -1
+
+
+def test_moe_router_host_checks(q):
+    p = _fake_ptr()
+    L = q.lib
+    for E, H, k, sh in ((0, 1024, 4, 0), (512, 96, 4, 0), (512, 1024, 0, 0), (512, 1024, 9, 0),
+                        (3, 1024, 4, -1), (512, 1024, 4, 512), (512, 1024, 4, -2)):
+        assert L.qgemv_moe_router(p, p, p, p, E, H, k, sh, p, p, p, None) == -1
+    for i in (0, 1, 2, 3, 8, 9, 10):
+        args = [p, p, p, p, 512, 1024, 4, 0, p, p, p]
+        args[i] = None
+        assert L.qgemv_moe_router(*args, None) == -2
+    two = _fake_ptr(0x10002)
+    assert L.qgemv_moe_router(p, p, p, p, 512, 1024, 4, 0, p, two, p, None) == -3
 
 
 def test_lm_head_argmax_host_checks(q):
