@@ -21,9 +21,14 @@
  * factored per group of 64: scale * sum(q*x) + bias * sum(x).
  *
  * Conventions.
- *   - Every pointer argument except `stream` is a DEVICE pointer owned by
- *     the caller.  The library never allocates, frees or synchronises; work
- *     is only enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Every pointer argument except `stream` (and the host descriptor
+ *     arrays of qgemv_decode_stack) is a DEVICE pointer owned by the caller.
+ *     The library allocates no device memory per call and does not
+ *     synchronise (qgemv_device_status excepted); work is only enqueued on
+ *     `stream` (a cudaStream_t; NULL = legacy default).  It holds three
+ *     things of its own for the life of the process: the fixed scratch
+ *     array of moe_qgemv_combine_noalloc, and the CUDA graphs (at most 4)
+ *     and the capture stream per device of qgemv_decode_stack.
  *   - Return value: QGEMV_OK (0) or a negative QGEMV_E* status.  Argument
  *     checks run on the host before any launch; on failure nothing is
  *     enqueued.  QGEMV_ELAUNCH reports a CUDA error seen right after the
