@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     qgemv_w2g64,
     qgemv_w4g64,
     qgemv_w8g64,
+    residual_rmsnorm,
     rmsnorm_qgemv,
     selftest_wait_timeout,
     strerror,

@@ -42,6 +42,7 @@ _SIGS = {
     "qgemv_lm_head_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "qgemv_argmax_scratch_bytes": (ctypes.c_size_t, []),
     "qgemv_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "qgemv_residual_rmsnorm": (_I, [_P, _P, _P, _F, _I, _P, _P, _P]),
 }
 
 #: Names the C header declares (the binding exposes each one).
@@ -136,6 +137,23 @@ def qgemv_w4g64(w, x, y=None, residual=None, stream=None):
 def qgemv_w2g64(w, x, y=None, residual=None, stream=None):
     """y = W x (+ residual) for a 2-bit g64 weight w = (codes, scales, biases)."""
     return _plain(lib.qgemv_w2g64, 2, w, x, y, residual, stream)
+
+
+def residual_rmsnorm(x, gamma, residual=None, eps=1e-5, h=None, xn=None, stream=None):
+    """qgemv_residual_rmsnorm: h = x + residual (fp16; x itself when residual
+    is None), xn = RMSNorm(h) * gamma (fp16).  Returns (h, xn)."""
+    x = _cuda(x, _F16, "x")
+    gamma = _cuda(gamma, _F16, "gamma")
+    _cuda(residual, _F16, "residual")
+    K = x.shape[-1]
+    if residual is not None and h is None:
+        h = torch.empty(K, dtype=torch.float16, device=x.device)
+    if xn is None:
+        xn = torch.empty(K, dtype=torch.float16, device=x.device)
+    st = lib.qgemv_residual_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), K, _ptr(h),
+                                    _ptr(xn), _stream(stream))
+    _check(st, "qgemv_residual_rmsnorm")
+    return (h if residual is not None else x), xn
 
 
 def moe_router(w, x, top_k=4, shared=0, logits=None, idx=None, wt=None, stream=None):

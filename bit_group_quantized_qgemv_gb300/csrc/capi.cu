@@ -9,6 +9,7 @@
 
 #include "qgemv.h"
 #include "qgemv_args.h"
+#include "epilogue_ops.h"
 
 namespace {
 
@@ -320,6 +321,21 @@ int qgemv_moe_router(const uint32_t* codes, const uint16_t* scales, const uint16
   return finish(qgemv::moe_route_launch(reinterpret_cast<const __half*>(logits), E, top_k,
                                         shared_expert, expert_idx, expert_w,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int qgemv_residual_rmsnorm(const uint16_t* x, const uint16_t* residual, const uint16_t* gamma,
+                           float eps, int K, uint16_t* h, uint16_t* xn, void* stream) {
+  if (!x || !gamma || !xn || (residual && !h)) return QGEMV_ENULL;
+  if (K < 1 || !(eps > 0.0f)) return QGEMV_EINVAL;
+  if (!aligned(x, 2) || !aligned(residual, 2) || !aligned(gamma, 2) || !aligned(h, 2) ||
+      !aligned(xn, 2))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  return finish(qgemv::residual_rmsnorm_launch(
+      reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(residual),
+      reinterpret_cast<const __half*>(gamma), eps, K, reinterpret_cast<__half*>(h),
+      reinterpret_cast<__half*>(xn), static_cast<cudaStream_t>(stream)));
 }
 
 size_t qgemv_argmax_scratch_bytes(void) { return 16; }

@@ -4,6 +4,7 @@
 // same fp16 roundings of the activations as the streaming kernel; slower
 // (activations are re-read from L1/L2 for every row).
 #include "qgemv_args.h"
+#include "epilogue_ops.h"
 #include "qgemv_device.cuh"
 
 namespace qgemv {
@@ -341,6 +342,57 @@ cudaError_t moe_route_launch(const __half* logits, int E, int top_k, int shared,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, moe_route_kernel, logits, E, top_k, shared, idx, wt);
+}
+
+// Residual add and RMSNorm as a standalone epilogue, one CTA of 1024
+// threads: h = fp16(x + r) (exact sum, one rounding), xn = fp16(h * gamma *
+// rstd(h)) with rstd = 1 / sqrt(mean(h^2) + eps) over the fp16 h.  r may be
+// null (then h = x and it is not stored).
+__global__ void __launch_bounds__(1024) residual_rmsnorm_kernel(
+    const __half* __restrict__ x, const __half* __restrict__ r, const __half* __restrict__ gamma,
+    float eps, int K, __half* __restrict__ h, __half* __restrict__ xn) {
+  __shared__ float s_red[32];
+  __shared__ float s_rstd;
+  pdl_launch_dependents();
+  pdl_wait();  // x and r may come from the previous kernel
+  float sq = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float v = __half2float(x[k]);
+    if (r != nullptr) {
+      const __half hv = __float2half_rn(v + __half2float(r[k]));
+      h[k] = hv;
+      v = __half2float(hv);
+    }
+    sq = fmaf(v, v, sq);
+  }
+  sq = warp_sum(sq);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = sq;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? s_red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) s_rstd = 1.0f / sqrtf(t / static_cast<float>(K) + eps);
+  }
+  __syncthreads();
+  const float rstd = s_rstd;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const float v = __half2float(r != nullptr ? h[k] : x[k]);
+    xn[k] = __float2half_rn(v * __half2float(gamma[k]) * rstd);
+  }
+}
+
+cudaError_t residual_rmsnorm_launch(const __half* x, const __half* r, const __half* gamma,
+                                    float eps, int K, __half* h, __half* xn, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, residual_rmsnorm_kernel, x, r, gamma, eps, K, h, xn);
 }
 
 // Self-test of the bounded waits: one thread waits on an mbarrier that no

@@ -282,6 +282,20 @@ int qgemv_last_cuda_error(void);
 int qgemv_device_status(unsigned *flags);
 
 /*
+ * qgemv_residual_rmsnorm -- the residual add and the RMSNorm of a pre-norm
+ * block as one standalone epilogue (INFERENCE_RESEARCH.md section 1: the
+ * residual+norm fusion), for callers whose matvecs do not fuse them:
+ *   h  = x + residual, rounded once to fp16 (h = x when residual is NULL,
+ *        and then h is not written and may be NULL),
+ *   xn = h * gamma / sqrt(mean(h^2) + eps), rounded once to fp16, the mean
+ *        over the fp16 h.
+ * x, residual, gamma, h, xn: fp16 [K] device.  Checks: K >= 1, eps > 0.
+ * One CTA, chained by programmatic dependent launch.
+ */
+int qgemv_residual_rmsnorm(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
+                           float eps, int K, uint16_t *h, uint16_t *xn, void *stream);
+
+/*
  * qgemv_moe_router -- MoE routing of one token on the GPU (the hada.io page,
  * topic 27758, "Architecture du modele": K active experts of E, one shared;
  * INFERENCE_RESEARCH.md section 1: keep the routing on the device):

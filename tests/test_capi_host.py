@@ -31,7 +31,7 @@ def test_header_lists_the_boundary():
               "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
               "decode_attention_seq1", "qgemv_device_status",
               "qgemv_selftest_wait_timeout", "qgemv_decode_stack", "qgemv_lm_head_argmax",
-              "qgemv_argmax_scratch_bytes", "qgemv_moe_router"]:
+              "qgemv_argmax_scratch_bytes", "qgemv_moe_router", "qgemv_residual_rmsnorm"]:
         assert n in names
 
 
@@ -83,6 +83,17 @@ def test_bad_scalar_status(q):
         assert q.lib.qgemv_selftest_wait_timeout(limit, None) == -1
     for N, K in ((0, 1024), (8, 96), (8, 0)):
         assert q.lib.qgemv_lm_head_argmax(p, p, p, p, p, N, K, p, p, None) == -1
+
+
+def test_residual_rmsnorm_host_checks(q):
+    p, odd = _fake_ptr(), _fake_ptr(0x10001)
+    L = q.lib
+    assert L.qgemv_residual_rmsnorm(p, None, p, 1e-5, 0, None, p, None) == -1
+    assert L.qgemv_residual_rmsnorm(p, None, p, 0.0, 64, None, p, None) == -1
+    assert L.qgemv_residual_rmsnorm(None, None, p, 1e-5, 64, None, p, None) == -2
+    assert L.qgemv_residual_rmsnorm(p, p, p, 1e-5, 64, None, p, None) == -2   # h needed
+    assert L.qgemv_residual_rmsnorm(p, None, p, 1e-5, 64, None, None, None) == -2
+    assert L.qgemv_residual_rmsnorm(p, odd, p, 1e-5, 64, p, p, None) == -3
 
 
 def test_moe_router_host_checks(q):

@@ -263,3 +263,20 @@ def test_attention_seq1_copies_value_heads(n_q, n_kv, d):
 
 def test_no_device_side_timeouts():
     assert q.device_status() == 0
+
+
+# ------------------------------------------------- residual + RMSNorm epilogue
+@pytest.mark.parametrize("K,with_res", [(4096, True), (1024, True), (14336, True), (333, True),
+                                        (4096, False), (1, True)])
+def test_residual_rmsnorm(K, with_res):
+    eps = 1e-5
+    x = X(K + 1, K)
+    r = X(K + 2, K) if with_res else None
+    gamma = synth.norm_gamma(synth.rng(200, K, 13), K)
+    h, xn = q.residual_rmsnorm(dev16(x), dev16(gamma), None if r is None else dev16(r), eps)
+    # h: the exact sum rounded once to fp16, bit for bit
+    h16 = (x.astype(np.float64) + r.astype(np.float64)).astype(np.float16) if with_res else x
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), h16.view(np.uint16))
+    xn64 = oracle.rmsnorm(h16, gamma, eps)
+    tol = (2.0 ** -11 + 1e-5) * np.abs(xn64) + 1e-7   # one fp16 rounding + fp32 sums
+    check(xn, xn64, tol, f"residual_rmsnorm K={K} res={with_res}")
