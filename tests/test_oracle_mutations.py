@@ -53,3 +53,61 @@ def test_pins_catch_mutant(name, tmp_path):
                           "no:cacheprovider", os.path.join(ROOT, "tests", "test_oracle.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout[-2000:]}"
+
+
+# The routing oracle is Python: its mutants are copies of oracle/__init__.py
+# with one edit in moe_route, run under the routing pins of test_oracle.py.
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
+ROUTE_MUTANTS = {
+    "tie_to_higher_index": ("if best < 0 or lv[e] > lv[best]:", "if best < 0 or lv[e] >= lv[best]:"),
+    "smallest_logits": ("if best < 0 or lv[e] > lv[best]:", "if best < 0 or lv[e] < lv[best]:"),
+    "shared_dropped": ("chosen = [int(shared)] if shared >= 0 else []", "chosen = []"),
+    "chosen_not_excluded": ("            if e in chosen:\n                continue\n", ""),
+    "weights_unnormalised": ("[v / tot for v in ex]", "[v for v in ex]"),
+    "hidden_temperature": ("float(np.exp(v - m))", "float(np.exp(2.0 * (v - m)))"),
+}
+
+_ROUTE_PINS = """
+import importlib.util, sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+spec = importlib.util.spec_from_file_location("oracle", {path!r},
+                                              submodule_search_locations=[{pkg!r}])
+mod = importlib.util.module_from_spec(spec); sys.modules["oracle"] = mod
+spec.loader.exec_module(mod)
+import test_oracle as t
+t.oracle = mod
+t.test_moe_route_hand_example()
+t.test_moe_route_equal_logits_and_no_shared_expert()
+for args in [(512, 4, 0), (64, 8, -1), (33, 1, 5), (16, 2, 15)]:
+    t.test_moe_route_against_stable_sort(*args)
+"""
+
+
+@pytest.mark.parametrize("name", sorted(ROUTE_MUTANTS))
+def test_route_pins_catch_mutant(name, tmp_path):
+    old, new = ROUTE_MUTANTS[name]
+    src = open(PY_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor missing: {old!r}"
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(src.replace(old, new))
+    script = _ROUTE_PINS.format(root=ROOT, tests=os.path.join(ROOT, "tests"),
+                                path=str(pkg / "__init__.py"), pkg=str(pkg))
+    # the C library the copy would build is the real one (only moe_route differs)
+    env = dict(os.environ, QGEMV_ORACLE_LIB=os.path.join(ROOT, "oracle", "_build", "liboracle.so"))
+    res = subprocess.run([sys.executable, "-c", script], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode != 0, f"routing mutant {name} passed every pin:\n{res.stdout[-1000:]}"
+
+
+def test_route_pins_pass_on_the_real_oracle(tmp_path):
+    # the harness itself: the unmutated copy passes
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(open(PY_SRC).read())
+    script = _ROUTE_PINS.format(root=ROOT, tests=os.path.join(ROOT, "tests"),
+                                path=str(pkg / "__init__.py"), pkg=str(pkg))
+    env = dict(os.environ, QGEMV_ORACLE_LIB=os.path.join(ROOT, "oracle", "_build", "liboracle.so"))
+    res = subprocess.run([sys.executable, "-c", script], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
