@@ -251,3 +251,19 @@ def moe_route(logits, top_k: int, shared: int = 0):
     ex = [float(np.exp(v - m)) for v in sel]
     tot = sum(ex)
     return np.array(chosen, np.int32), np.array([v / tot for v in ex], np.float64)
+
+
+def lm_head_sample(logits, top_k: int, temperature: float, u: float):
+    """Top-k sampling of the next token from its logits (INFERENCE_RESEARCH.md
+    section 1: lm_head and top-k sampling on the GPU, only the token read
+    back; the random number u in [0, 1) is an input): the top_k largest fp16
+    logits, ties to the lower index, in decreasing order; weights
+    p_j = exp((l_j - l_0) / temperature) in fp64; the token is the first
+    candidate whose cumulative weight exceeds u * sum(p).  Returns (token,
+    candidates int64 [top_k], cumulative weights / sum float64 [top_k])."""
+    lv = np.asarray(logits, np.float16).astype(np.float64)
+    cand = np.argsort(-lv, kind="stable")[:top_k]      # a library sort as the selection step
+    p = np.exp((lv[cand] - lv[cand[0]]) / float(temperature))
+    cum = np.cumsum(p) / p.sum()
+    j = int(np.argmax(cum > float(u))) if np.any(cum > float(u)) else top_k - 1
+    return int(cand[j]), cand.astype(np.int64), cum

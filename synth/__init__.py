@@ -14,11 +14,11 @@ Tensor ids (the third seed word):
     5 down                    6 lm_head          7 MoE gate.up  8 MoE down
     10 x (activation)         11 residual        12 norm gamma (first norm)
     13 norm gamma (second)    14 MoE routing     15 spare weight
-    16 MoE router weight
+    16 MoE router weight      17 logits          18 sampling uniforms
 
 Workloads (the first seed word): 0 the 1024 x 1024 GEMV, 1 the
 Llama-3.1-8B-shaped layer, 2 the Qwen3-0.6B-shaped stack, 3 the MoE, 4 the
-2-bit layer and small batches, 5 the 8-bit (Q8) layer.
+2-bit layer and small batches, 5 the 8-bit (Q8) layer, 6 top-k sampling.
 """
 from __future__ import annotations
 
@@ -29,7 +29,8 @@ import numpy as np
 TID = {
     "qkv": 1, "o": 2, "gate": 3, "up": 4, "down": 5, "lm_head": 6,
     "moe_gu": 7, "moe_down": 8, "x": 10, "residual": 11, "gamma1": 12,
-    "gamma2": 13, "routing": 14, "spare": 15, "router": 16,
+    "gamma2": 13, "routing": 14, "spare": 15, "router": 16, "logits": 17,
+    "u": 18,
 }
 
 
@@ -115,6 +116,25 @@ def routing(g: np.random.Generator, n_experts: int, top_k: int = 4,
     ex = np.exp(logits - logits.max())
     wt = (ex / ex.sum()).astype(np.float32)
     return idx, wt
+
+
+def logits(g: np.random.Generator, N: int, spread: float = 2.5, peaks: int = 8,
+           step: float | None = None) -> np.ndarray:
+    """fp16 next-token logits [N]: N(0, spread) with ``peaks`` entries raised
+    by U(6, 12) (a few likely tokens); with ``step``, every value is rounded
+    to a multiple of it (many exact ties)."""
+    v = g.normal(0.0, spread, size=N)
+    if peaks:
+        at = g.choice(N, size=min(peaks, N), replace=False)
+        v[at] += g.uniform(6.0, 12.0, size=at.size)
+    if step is not None:
+        v = np.round(v / step) * step
+    return v.astype(np.float16)
+
+
+def uniforms(g: np.random.Generator, n: int) -> np.ndarray:
+    """fp32 uniforms in [0, 1) (the random numbers a sampler is given)."""
+    return g.random(n, dtype=np.float32)
 
 
 # ------------------------------------------------------------------ shapes

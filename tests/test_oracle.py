@@ -426,3 +426,40 @@ def test_moe_route_against_stable_sort(E, top_k, shared):
     # the softmax of the chosen logits, ranked like them
     assert np.allclose(wt, np.exp(sel - sel.max()) / np.exp(sel - sel.max()).sum(), rtol=1e-14)
     assert np.all(np.diff(wt[1 if shared >= 0 else 0:]) <= 1e-15)
+
+
+# ------------------------------------------------------ top-k sampling
+def test_lm_head_sample_hand_example():
+    # logits 1, 3, 2, 3: top 3 = indices 1 and 3 (tie at 3.0, lower first),
+    # then 2; weights 1, 1, e^-1 at T = 1
+    logits = np.array([1.0, 3.0, 2.0, 3.0], np.float16)
+    tot = 2.0 + np.exp(-1.0)
+    for u, want in ((0.2, 1), (0.5, 3), (0.9, 2), (0.0, 1)):
+        tok, cand, cum = oracle.lm_head_sample(logits, 3, 1.0, u)
+        assert tok == want and cand.tolist() == [1, 3, 2]
+        assert np.allclose(cum, np.array([1.0, 2.0, tot]) / tot, rtol=1e-15)
+
+
+def test_lm_head_sample_top1_is_greedy_and_temperature():
+    g = np.random.default_rng(7)
+    logits = g.normal(0, 2, 1000).astype(np.float16)
+    best = int(np.argmax(logits))
+    for u in (0.0, 0.5, 0.999):
+        assert oracle.lm_head_sample(logits, 1, 0.7, u)[0] == best
+    # a tiny temperature puts all the weight on the largest logit
+    assert oracle.lm_head_sample(logits, 40, 1e-4, 0.999)[0] == best
+
+
+def test_lm_head_sample_frequencies_follow_the_softmax():
+    # a fine grid of u visits each candidate in proportion to its weight
+    logits = np.array([0.0, 1.0, 0.5, -1.0, 2.0, 1.0], np.float16)
+    k, T = 4, 0.8
+    us = (np.arange(20000) + 0.5) / 20000
+    toks = [oracle.lm_head_sample(logits, k, T, u)[0] for u in us]
+    _, cand, _ = oracle.lm_head_sample(logits, k, T, 0.0)
+    lv = logits.astype(np.float64)[cand]
+    p = np.exp((lv - lv.max()) / T)
+    p /= p.sum()
+    freq = np.array([toks.count(int(c)) for c in cand]) / len(us)
+    assert cand.tolist() == [4, 1, 5, 2]
+    assert np.allclose(freq, p, atol=1e-4)
