@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--op", default="stack",
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, moe_routed, lm_head, lm_head_argmax, "
-                        "gemv1024, "
+                        "lm_head_sample, gemv1024, "
                         "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
@@ -471,7 +471,7 @@ def run_own(args):
 
 
 OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "moe_routed", "lm_head", "lm_head_argmax",
-       "gemv1024",
+       "lm_head_sample", "gemv1024",
        "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2"]
 
 
@@ -563,13 +563,17 @@ def run_one_op(args, name):
             if name == "moe_routed":
                 q.moe_router(w[2], x, top_k=4, shared=0, logits=rlog, idx=idx, wt=wt)
             q.moe_qgemv_combine(w[0], w[1], idx, wt, x, x, y=y, workspace=work)
-    elif name in ("lm_head", "lm_head_argmax", "gemv1024"):
+    elif name in ("lm_head", "lm_head_argmax", "lm_head_sample", "gemv1024"):
         if name == "lm_head":
             config = "config 2: Qwen3-0.6B-shaped lm_head 1024->151936"
             N, K, wl = cq["vocab"], cq["hidden"], 2
         elif name == "lm_head_argmax":
             config = ("config 2: Qwen3-0.6B-shaped lm_head 1024->151936 with the greedy token "
                       "chosen on the GPU")
+            N, K, wl = cq["vocab"], cq["hidden"], 2
+        elif name == "lm_head_sample":
+            config = ("config 2: Qwen3-0.6B-shaped lm_head 1024->151936 with top-k sampling "
+                      "(k = 50, temperature 0.8) on the GPU")
             N, K, wl = cq["vocab"], cq["hidden"], 2
         else:
             config = "config 0: single 4-bit g64 GEMV 1024x1024"
@@ -581,13 +585,16 @@ def run_one_op(args, name):
         y = torch.empty(N, device=dev).half()
         am_scratch = torch.zeros(q.argmax_scratch_bytes(), dtype=torch.uint8, device=dev)
         am_token = torch.empty(1, dtype=torch.int32, device=dev)
+        u = torch.from_numpy(synth.uniforms(synth.rng(6, 0, synth.TID["u"]), 1)).to(dev)
 
         def call(w):
             if name == "lm_head_argmax":
                 q.lm_head_argmax(w[0], x, logits=y, scratch=am_scratch, token=am_token)
+            elif name == "lm_head_sample":
+                q.lm_head_sample(w[0], x, 50, 0.8, u, logits=y, token=am_token)
             else:
                 q.qgemv_w4g64(w[0], x, y=y)
-        launches = 1
+        launches = 1 if name in ("lm_head", "gemv1024") else 2
     elif name in ("w2_layer", "w8_layer"):
         wb = 2 if name == "w2_layer" else 8
         config = ("config 4: the five matvecs of one 8B-shaped layer at 2-bit" if wb == 2 else

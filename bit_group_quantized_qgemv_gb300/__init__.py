@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     last_cuda_error,
     lib,
     lm_head_argmax,
+    lm_head_sample,
     argmax_scratch_bytes,
     moe_qgemv_combine,
     moe_router,
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     qgemv_w8g64,
     residual_rmsnorm,
     rmsnorm_qgemv,
+    sample_topk,
     selftest_wait_timeout,
     strerror,
     swiglu_qgemv,

@@ -43,6 +43,8 @@ _SIGS = {
     "qgemv_argmax_scratch_bytes": (ctypes.c_size_t, []),
     "qgemv_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "qgemv_residual_rmsnorm": (_I, [_P, _P, _P, _F, _I, _P, _P, _P]),
+    "qgemv_sample_topk": (_I, [_P, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "qgemv_lm_head_sample": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
 }
 
 #: Names the C header declares (the binding exposes each one).
@@ -205,6 +207,57 @@ def lm_head_argmax(w, x, logits=None, scratch=None, token=None, stream=None):
                                   N, K, _ptr(scratch), _ptr(token), _stream(stream))
     _check(st, "qgemv_lm_head_argmax")
     return token, logits
+
+
+def _sample_outputs(device, top_k, u, token, want_topk, topk_idx, topk_prob):
+    u = _cuda(u, (torch.float32,), "u")
+    if token is None:
+        token = torch.empty(1, dtype=torch.int32, device=device)
+    _cuda(token, (torch.int32,), "token")
+    if want_topk:
+        if topk_idx is None:
+            topk_idx = torch.empty(top_k, dtype=torch.int32, device=device)
+        if topk_prob is None:
+            topk_prob = torch.empty(top_k, dtype=torch.float32, device=device)
+    _cuda(topk_idx, (torch.int32,), "topk_idx")
+    _cuda(topk_prob, (torch.float32,), "topk_prob")
+    return u, token, topk_idx, topk_prob
+
+
+def sample_topk(logits, top_k, temperature, u, token=None, want_topk=False, topk_idx=None,
+                topk_prob=None, stream=None):
+    """Top-k sampling on the device (qgemv_sample_topk) from fp16 logits [N];
+    u: fp32 [1] on the device (the caller's random number in [0, 1)).
+    Returns (token int32 [1], topk_idx int32 [top_k] or None, topk_prob fp32
+    [top_k] or None); the candidate outputs are made when want_topk."""
+    logits = _cuda(logits, _F16, "logits")
+    u, token, topk_idx, topk_prob = _sample_outputs(logits.device, top_k, u, token, want_topk,
+                                                    topk_idx, topk_prob)
+    st = lib.qgemv_sample_topk(_ptr(logits), logits.numel(), int(top_k), float(temperature),
+                               _ptr(u), _ptr(token), _ptr(topk_idx), _ptr(topk_prob),
+                               _stream(stream))
+    _check(st, "qgemv_sample_topk")
+    return token, topk_idx, topk_prob
+
+
+def lm_head_sample(w, x, top_k, temperature, u, logits=None, token=None, want_topk=False,
+                   topk_idx=None, topk_prob=None, stream=None):
+    """lm_head matvec (4-bit g64) then top-k sampling (qgemv_lm_head_sample).
+    Returns (token, logits, topk_idx, topk_prob) as sample_topk."""
+    codes, scales, biases = _weight(w, "w")
+    x = _cuda(x, _F16, "x")
+    N = codes.shape[-2]
+    K = codes.shape[-1] * 8  # 4-bit: 8 codes per 32-bit word
+    if logits is None:
+        logits = torch.empty(N, dtype=torch.float16, device=x.device)
+    _cuda(logits, _F16, "logits")
+    u, token, topk_idx, topk_prob = _sample_outputs(x.device, top_k, u, token, want_topk,
+                                                    topk_idx, topk_prob)
+    st = lib.qgemv_lm_head_sample(_ptr(codes), _ptr(scales), _ptr(biases), _ptr(x),
+                                  _ptr(logits), N, K, int(top_k), float(temperature), _ptr(u),
+                                  _ptr(token), _ptr(topk_idx), _ptr(topk_prob), _stream(stream))
+    _check(st, "qgemv_lm_head_sample")
+    return token, logits, topk_idx, topk_prob
 
 
 def qgemv_w8g64(w, x, y=None, residual=None, stream=None):

@@ -6,10 +6,14 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cmath>
 
 #include "qgemv.h"
 #include "qgemv_args.h"
 #include "epilogue_ops.h"
+
+static_assert(QGEMV_SAMPLE_MAX_K == qgemv::kMaxSampleK, "sampler candidate limit");
+static_assert(QGEMV_SAMPLE_MAX_N == qgemv::kMaxSampleN, "sampler logits limit");
 
 namespace {
 
@@ -43,6 +47,18 @@ int finish(cudaError_t e) {
 }
 
 bool valid_k(int K) { return K >= 64 && K % 64 == 0; }
+
+int check_sample(const uint16_t* logits, int N, int top_k, float temperature, const float* u,
+                 const int32_t* token, const int32_t* topk_idx, const float* topk_prob) {
+  if (!logits || !u || !token) return QGEMV_ENULL;
+  if (N < 1 || N > QGEMV_SAMPLE_MAX_N || top_k < 1 || top_k > QGEMV_SAMPLE_MAX_K || top_k > N)
+    return QGEMV_EINVAL;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return QGEMV_EINVAL;
+  if (!aligned(logits, 2) || !aligned(u, 4) || !aligned(token, 4) || !aligned(topk_idx, 4) ||
+      !aligned(topk_prob, 4))
+    return QGEMV_EALIGN;
+  return QGEMV_OK;
+}
 
 StreamArgs blank_args() {
   StreamArgs a{};
@@ -371,6 +387,32 @@ int qgemv_lm_head_argmax(const uint32_t* codes, const uint16_t* scales, const ui
   const cudaError_t e = qgemv::generic_launch(qgemv::kPlain, 4, a, st);
   if (e != cudaSuccess) return finish(e);
   return finish(qgemv::argmax_launch(a.y, N, token, st));
+}
+
+int qgemv_sample_topk(const uint16_t* logits, int N, int top_k, float temperature,
+                      const float* u, int32_t* token, int32_t* topk_idx, float* topk_prob,
+                      void* stream) {
+  if (int rc = check_sample(logits, N, top_k, temperature, u, token, topk_idx, topk_prob)) return rc;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  return finish(qgemv::sample_topk_launch(reinterpret_cast<const __half*>(logits), N, top_k,
+                                          temperature, u, token, topk_idx, topk_prob,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int qgemv_lm_head_sample(const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
+                         const uint16_t* x, uint16_t* logits, int N, int K, int top_k,
+                         float temperature, const float* u, int32_t* token, int32_t* topk_idx,
+                         float* topk_prob, void* stream) {
+  if (!codes || !scales || !biases || !x) return QGEMV_ENULL;
+  if (int rc = check_sample(logits, N, top_k, temperature, u, token, topk_idx, topk_prob)) return rc;
+  if (!valid_k(K)) return QGEMV_EINVAL;
+  if (!aligned(codes, 4) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(x, 2))
+    return QGEMV_EALIGN;
+  if (int rc = plain_impl(4, codes, scales, biases, x, logits, 1, N, K, nullptr, stream)) return rc;
+  return finish(qgemv::sample_topk_launch(reinterpret_cast<const __half*>(logits), N, top_k,
+                                          temperature, u, token, topk_idx, topk_prob,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int qgemv_selftest_wait_timeout(unsigned limit_us, void* stream) {

@@ -338,6 +338,47 @@ int qgemv_lm_head_argmax(const uint32_t *codes, const uint16_t *scales, const ui
 /* Bytes of the scratch qgemv_lm_head_argmax needs (16). */
 size_t qgemv_argmax_scratch_bytes(void);
 
+#define QGEMV_SAMPLE_MAX_K 1024
+#define QGEMV_SAMPLE_MAX_N 786432
+
+/*
+ * qgemv_sample_topk -- top-k sampling of the next token from its logits on
+ * the GPU (INFERENCE_RESEARCH.md section 1: the logits matvec followed by
+ * top-k sampling on the GPU, only the token read back).  The candidates are
+ * the top_k largest logits (the fp16 values compared, -0 equal to +0, the
+ * lower index first among equal values), in decreasing order c_0 .. c_{k-1};
+ * their weights p_j = exp((l[c_j] - l[c_0]) / temperature) (fp32); *token =
+ * c_j for the first j whose running sum p_0 + .. + p_j exceeds
+ * (*u) * (p_0 + .. + p_{k-1}), c_{k-1} when none does.  The random number is
+ * the caller's: u is one fp32 on the device, read when the kernel runs (so a
+ * captured graph samples afresh when the caller rewrites it), meant to be in
+ * [0, 1).  The choice of candidates is exact; the weights are fp32, so a u
+ * within about 1e-4 of a boundary of the running sum may fall to either
+ * neighbour.  logits: fp16 [N] device; token: int32 device; topk_idx (int32
+ * [top_k]) and topk_prob (fp32 [top_k], p_j / sum p) are optional device
+ * outputs (NULL to skip).  Logits are expected finite: a non-finite logit
+ * still yields one of the candidates, with unspecified weights.  Checks:
+ * 1 <= N <= QGEMV_SAMPLE_MAX_N, 1 <= top_k <= min(N, QGEMV_SAMPLE_MAX_K),
+ * temperature finite and > 0.  One launch of a cluster of 8 CTAs (each holds
+ * N/8 logits in shared memory), chained to the previous kernel on `stream`
+ * by programmatic dependent launch; no scratch, no allocation.
+ */
+int qgemv_sample_topk(const uint16_t *logits, int N, int top_k, float temperature,
+                      const float *u, int32_t *token, int32_t *topk_idx, float *topk_prob,
+                      void *stream);
+
+/*
+ * qgemv_lm_head_sample -- the lm_head matvec and top-k sampling as one call:
+ * logits = W . x exactly as qgemv_w4g64 (M = 1; logits fp16 [N] device
+ * output, required), then qgemv_sample_topk on those logits.  Arguments as
+ * the two calls; every check of both is made before the first launch.  Two
+ * launches, the second chained by programmatic dependent launch.
+ */
+int qgemv_lm_head_sample(const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                         const uint16_t *x, uint16_t *logits, int N, int K, int top_k,
+                         float temperature, const float *u, int32_t *token, int32_t *topk_idx,
+                         float *topk_prob, void *stream);
+
 /*
  * qgemv_selftest_wait_timeout -- health check of the bounded device waits
  * every kernel uses: enqueues one tiny kernel on `stream` whose thread waits

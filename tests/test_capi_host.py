@@ -31,7 +31,8 @@ def test_header_lists_the_boundary():
               "moe_qgemv_combine", "qgemv_moe_workspace_bytes", "qgemv_strerror",
               "decode_attention_seq1", "qgemv_device_status",
               "qgemv_selftest_wait_timeout", "qgemv_decode_stack", "qgemv_lm_head_argmax",
-              "qgemv_argmax_scratch_bytes", "qgemv_moe_router", "qgemv_residual_rmsnorm"]:
+              "qgemv_argmax_scratch_bytes", "qgemv_moe_router", "qgemv_residual_rmsnorm",
+              "qgemv_sample_topk", "qgemv_lm_head_sample"]:
         assert n in names
 
 
@@ -120,6 +121,31 @@ def test_lm_head_argmax_host_checks(q):
     assert L.qgemv_lm_head_argmax(p, p, p, p, p, 8, 64, four, p, None) == -3   # scratch: 8 B
     assert L.qgemv_lm_head_argmax(p, p, p, p, p, 8, 64, p, two, None) == -3    # token: 4 B
     assert q.argmax_scratch_bytes() == 16
+
+
+def test_sample_topk_host_checks(q):
+    p, two = _fake_ptr(), _fake_ptr(0x10002)
+    L = q.lib
+    inf, nan = float("inf"), float("nan")
+    for N, k, T in ((0, 1, 1.0), (786433, 1, 1.0), (100, 0, 1.0), (100, 101, 1.0),
+                    (5000, 1025, 1.0), (100, 5, 0.0), (100, 5, -1.0), (100, 5, inf),
+                    (100, 5, nan)):
+        assert L.qgemv_sample_topk(p, N, k, T, p, p, None, None, None) == -1
+        assert L.qgemv_lm_head_sample(p, p, p, p, p, N, 64, k, T, p, p, None, None, None) == -1
+    for i in (0, 4, 5):                      # logits, u, token are required
+        args = [p, 100, 5, 1.0, p, p, p, p]
+        args[i] = None
+        assert L.qgemv_sample_topk(*args, None) == -2
+    for i in (0, 1, 2, 3, 4, 9, 10):         # + the weight and x
+        args = [p, p, p, p, p, 100, 64, 5, 1.0, p, p, p, p]
+        args[i] = None
+        assert L.qgemv_lm_head_sample(*args, None) == -2
+    assert L.qgemv_lm_head_sample(p, p, p, p, p, 100, 96, 5, 1.0, p, p, None, None, None) == -1
+    for i in (4, 5, 6, 7):                   # u, token, topk_idx, topk_prob: 4 B
+        args = [p, 100, 5, 1.0, p, p, p, p]
+        args[i] = two
+        assert L.qgemv_sample_topk(*args, None) == -3
+    assert L.qgemv_sample_topk(_fake_ptr(0x10001), 100, 5, 1.0, p, p, None, None, None) == -3
 
 
 def test_misaligned_status(q):
