@@ -463,3 +463,16 @@ def test_lm_head_sample_frequencies_follow_the_softmax():
     freq = np.array([toks.count(int(c)) for c in cand]) / len(us)
     assert cand.tolist() == [4, 1, 5, 2]
     assert np.allclose(freq, p, atol=1e-4)
+
+
+def test_lm_head_sample_boundaries():
+    # two equal logits: running sums exactly 0.5 and 1.0, so u = 0.5 is not
+    # exceeded by the first (the pick needs a strictly larger running sum)
+    lv = np.array([2.0, 2.0, -1.0], np.float16)
+    assert oracle.lm_head_sample(lv, 2, 1.0, 0.5)[0] == 1
+    assert oracle.lm_head_sample(lv, 2, 1.0, 0.4999)[0] == 0
+    # no running sum exceeds u >= 1: the last candidate
+    assert oracle.lm_head_sample(lv, 3, 1.0, 1.0)[0] == 2
+    # ties among the top values go to the lower index even when they are not first
+    lv = np.array([0.0, 1.0, 3.0, 1.0, 1.0], np.float16)
+    assert oracle.lm_head_sample(lv, 3, 1.0, 0.0)[1].tolist() == [2, 1, 3]

@@ -111,3 +111,53 @@ def test_route_pins_pass_on_the_real_oracle(tmp_path):
     res = subprocess.run([sys.executable, "-c", script], cwd=ROOT, env=env,
                          capture_output=True, text=True, timeout=300)
     assert res.returncode == 0, res.stderr[-2000:]
+
+
+# Planted mistakes in the top-k sampling oracle; the sampling pins must fail
+# on each.
+SAMPLE_MUTANTS = {
+    "tie_to_higher_index": ('cand = np.argsort(-lv, kind="stable")[:top_k]',
+                            'cand = (len(lv) - 1 - np.argsort(-lv[::-1], kind="stable"))[:top_k]'),
+    "smallest_logits": ('cand = np.argsort(-lv, kind="stable")[:top_k]',
+                        'cand = np.argsort(lv, kind="stable")[:top_k]'),
+    "one_candidate_short": ('cand = np.argsort(-lv, kind="stable")[:top_k]',
+                            'cand = np.argsort(-lv, kind="stable")[:max(top_k - 1, 1)]'),
+    "temperature_multiplies": ("/ float(temperature))", "* float(temperature))"),
+    "running_sum_unnormalised": ("cum = np.cumsum(p) / p.sum()", "cum = np.cumsum(p)"),
+    "pick_at_equal_sum": ("j = int(np.argmax(cum > float(u))) if np.any(cum > float(u))",
+                          "j = int(np.argmax(cum >= float(u))) if np.any(cum >= float(u))"),
+    "fallback_to_first": ("else top_k - 1", "else 0"),
+}
+
+_SAMPLE_PINS = _ROUTE_PINS.split("import test_oracle as t")[0] + """import test_oracle as t
+t.oracle = mod
+t.test_lm_head_sample_hand_example()
+t.test_lm_head_sample_top1_is_greedy_and_temperature()
+t.test_lm_head_sample_frequencies_follow_the_softmax()
+t.test_lm_head_sample_boundaries()
+"""
+
+
+def _run_pins(script_tmpl, src, tmp_path):
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    (pkg / "__init__.py").write_text(src)
+    script = script_tmpl.format(root=ROOT, tests=os.path.join(ROOT, "tests"),
+                                path=str(pkg / "__init__.py"), pkg=str(pkg))
+    env = dict(os.environ, QGEMV_ORACLE_LIB=os.path.join(ROOT, "oracle", "_build", "liboracle.so"))
+    return subprocess.run([sys.executable, "-c", script], cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=300)
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLE_MUTANTS))
+def test_sample_pins_catch_mutant(name, tmp_path):
+    old, new = SAMPLE_MUTANTS[name]
+    src = open(PY_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor missing: {old!r}"
+    res = _run_pins(_SAMPLE_PINS, src.replace(old, new), tmp_path)
+    assert res.returncode != 0, f"sampling mutant {name} passed every pin:\n{res.stdout[-1000:]}"
+
+
+def test_sample_pins_pass_on_the_real_oracle(tmp_path):
+    res = _run_pins(_SAMPLE_PINS, open(PY_SRC).read(), tmp_path)
+    assert res.returncode == 0, res.stderr[-2000:]
