@@ -60,6 +60,7 @@ _SIGS = {
                                    _P, _P, _P]),
     "oracle_moe_qgemv_combine": (None, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P,
                                         _P, _I, _P, _P, _P, _P, _P, _P]),
+    "oracle_lut_qgemv": (None, [_P, _P, _I, _P, _P, _I, _I, _P, _P, _P]),
 }
 
 
@@ -161,6 +162,26 @@ def qgemv(bits, codes, scales, biases, x, residual=None):
     if squeeze:
         return y64[0], y16[0], bound[0]
     return y64, y16, bound
+
+
+def lut_qgemv(codes, lut, rows_per_lut, x, residual=None):
+    """LUT / palettised 4-bit GEMV (INFERENCE_RESEARCH.md section 3, item 4:
+    4-bit indices and a 16-entry fp16 table, Core ML style):
+    y[n] = sum_k lut[n // rows_per_lut][q[n][k]] x[k] (+ residual[n]).
+    codes uint32 [N][K/8]; lut fp16 [ceil(N / rows_per_lut)][16]; x fp16
+    [K].  Returns (y64, y16 as float16, bound = sum |w||x| + |residual|)."""
+    codes = _u32(codes)
+    lb = _f16bits(lut).reshape(-1, 16)
+    xb = _f16bits(x).reshape(-1)
+    N, K = codes.shape[0], xb.shape[0]
+    assert codes.shape[1] * 8 == K and lb.shape[0] * rows_per_lut >= N
+    rb = None if residual is None else _f16bits(residual).reshape(N)
+    y64 = np.empty(N, np.float64)
+    y16 = np.empty(N, np.uint16)
+    bound = np.empty(N, np.float64)
+    lib().oracle_lut_qgemv(_ptr(codes), _ptr(lb), int(rows_per_lut), _ptr(xb), _ptr(rb), N, K,
+                           _ptr(y64), _ptr(y16), _ptr(bound))
+    return y64, y16.view(np.float16), bound
 
 
 def rmsnorm(x, gamma, eps):

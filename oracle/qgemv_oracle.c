@@ -24,6 +24,11 @@
  *     page, "Noyau de dequantification optimise FMA" ((nibble*scale+bias)*x,
  *     rewritten as fma(nibble, scale*x, bias*x); an exact identity, so the
  *     oracle evaluates the plain product).
+ *   - LUT / palettised 4-bit weights: the same 4-bit codes index a table
+ *     of 16 fp16 values, w = lut[q]; INFERENCE_RESEARCH.md section 3,
+ *     item 4 (add a LUT/palettised type: 4-bit indices plus a 16-entry
+ *     f16 LUT, Core ML style).  One table serves rows_per_lut consecutive
+ *     rows (all N: one table per tensor; 1: one per row).
  *   - Fusions RMSNorm->QKV, gate.up SwiGLU, MoE combine + residual:
  *     INFERENCE_RESEARCH.md section 1 (fusions to implement) and the hada.io
  *     page, "Shaders de calcul Metal" and "Deferred GPU Expert Compute".
@@ -209,6 +214,42 @@ void oracle_qgemv(int bits, const uint32_t *codes, const uint16_t *scales,
     free(xd);
     free(yd);
     free(ab);
+}
+
+/* ------------------------------------------------ LUT / palettised */
+
+/*
+ * y[n] = sum_k lut[n / rows_per_lut][q[n][k]] * x[k] (+ residual[n]) for
+ * 4-bit codes q (8 per uint32, low nibble first) and fp16 tables of 16
+ * entries.  y64 = the fp64 value, y16 its fp16 rounding, bound = sum |w||x|
+ * + |residual|.  Any of y64, y16, bound may be NULL.
+ */
+void oracle_lut_qgemv(const uint32_t *codes, const uint16_t *lut, int rows_per_lut,
+                      const uint16_t *x, const uint16_t *residual, int N, int K,
+                      double *y64, uint16_t *y16, double *bound)
+{
+    int nt = oracle_get_threads();
+    (void)nt;
+#pragma omp parallel for schedule(static) num_threads(nt)
+    for (int n = 0; n < N; ++n) {
+        const uint32_t *row = codes + (int64_t)n * words_per_row(4, K);
+        const uint16_t *table = lut + (int64_t)(n / rows_per_lut) * 16;
+        double acc = 0.0, mag = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double w = oracle_half_to_double(table[oracle_code(row, 4, k)]);
+            double xv = oracle_half_to_double(x[k]);
+            acc += w * xv;
+            mag += fabs(w) * fabs(xv);
+        }
+        if (residual) {
+            double r = oracle_half_to_double(residual[n]);
+            acc += r;
+            mag += fabs(r);
+        }
+        if (y64) y64[n] = acc;
+        if (y16) y16[n] = oracle_double_to_half(acc);
+        if (bound) bound[n] = mag;
+    }
 }
 
 /* ----------------------------------------------------------- RMSNorm */

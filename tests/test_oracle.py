@@ -476,3 +476,101 @@ def test_lm_head_sample_boundaries():
     # ties among the top values go to the lower index even when they are not first
     lv = np.array([0.0, 1.0, 3.0, 1.0, 1.0], np.float16)
     assert oracle.lm_head_sample(lv, 3, 1.0, 0.0)[1].tolist() == [2, 1, 3]
+
+
+# ------------------------------------------------------ LUT / palettised
+def _unpack4(codes):
+    """Byte-view unpack of 4-bit codes, low nibble first (independent of the
+    oracle's oracle_code)."""
+    b = np.ascontiguousarray(codes).view(np.uint8)
+    return np.stack([b & 15, b >> 4], axis=-1).reshape(codes.shape[0], -1).astype(np.int64)
+
+
+def _lut_fixture():
+    d = load_golden("hand_example_d_lut.txt")
+    w0 = [int(w, 16) for w in d["words0"].split()]
+    w1 = [int(w, 16) for w in d["words1"].split()]
+    codes = np.array([w0, w1], np.uint32)
+    lut = np.array([[float(v) for v in d["lut0"].split()],
+                    [float(v) for v in d["lut1"].split()]], np.float16)
+    K = int(d["K"])
+    x = np.where(np.arange(K) % 2 == 0, float(d["x_even"]), float(d["x_odd"])).astype(np.float16)
+    return d, codes, lut, x
+
+
+def test_lut_hand_example_d():
+    d, codes, lut, x = _lut_fixture()
+    y64, y16, bound = oracle.lut_qgemv(codes, lut, 1, x)
+    assert y64.tolist() == [float(v) for v in d["y"].split()]
+    assert y16.astype(np.float64).tolist() == [float(v) for v in d["y"].split()]
+    assert bound.tolist() == [float(v) for v in d["bound"].split()]
+    # one table for both rows
+    y64s, _, _ = oracle.lut_qgemv(codes, lut[:1], 2, x)
+    assert y64s[1] == float(d["y1_shared_table"]) and y64s[0] == y64[0]
+    # the fixture's misread value is what reading the nibbles high first gives
+    q = _unpack4(codes)[1]
+    q_hi = q.reshape(-1, 8)[:, ::-1].reshape(-1)
+    lv = lut[1].astype(np.float64)
+    assert np.dot(lv[q_hi], x.astype(np.float64)) == float(d["y1_high_nibble_first"])
+
+
+@pytest.mark.parametrize("N,K,R,seed", [(7, 64, 1, 1), (33, 192, 4, 2), (16, 1024, 16, 3),
+                                        (5, 128, 3, 4)])
+def test_lut_brute_force(N, K, R, seed):
+    g = np.random.default_rng(seed)
+    codes = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    lut = g.normal(0, 0.05, size=(-(-N // R), 16)).astype(np.float16)
+    x = g.normal(0, 1, size=K).astype(np.float16)
+    r = g.normal(0, 1, size=N).astype(np.float16)
+    w = lut.astype(np.float64)[np.arange(N)[:, None] // R, _unpack4(codes)]
+    want = w @ x.astype(np.float64) + r.astype(np.float64)
+    y64, y16, bound = oracle.lut_qgemv(codes, lut, R, x, r)
+    assert np.allclose(y64, want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bound, np.abs(w) @ np.abs(x.astype(np.float64)) + np.abs(r.astype(np.float64)),
+                       rtol=1e-12)
+    assert np.array_equal(y16, want.astype(np.float16))
+
+
+def test_lut_affine_table_is_the_q4_format():
+    # lut[v] = v * s + b (exact in fp16) is the 4-bit g64 format with that
+    # scale and bias in every group of the row
+    g = np.random.default_rng(11)
+    N, K = 9, 256
+    codes = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    s = (g.integers(1, 64, size=N) / 256).astype(np.float16)
+    b = (-g.integers(0, 64, size=N) / 64).astype(np.float16)
+    lut = (np.arange(16)[None, :] * s.astype(np.float64)[:, None]
+           + b.astype(np.float64)[:, None]).astype(np.float16)
+    assert np.array_equal(lut.astype(np.float64),
+                          np.arange(16)[None, :] * s.astype(np.float64)[:, None]
+                          + b.astype(np.float64)[:, None])
+    x = g.normal(0, 1, size=K).astype(np.float16)
+    y_lut, _, _ = oracle.lut_qgemv(codes, lut, 1, x)
+    sc = np.repeat(s[:, None], K // 64, axis=1)
+    bi = np.repeat(b[:, None], K // 64, axis=1)
+    y_q4, _, _ = oracle.qgemv(4, codes, sc, bi, x)
+    assert np.allclose(y_lut, y_q4, rtol=1e-13, atol=1e-13)
+
+
+def test_lut_relabelling_and_shared_tables():
+    g = np.random.default_rng(12)
+    N, K = 12, 512
+    codes = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    lut = g.normal(0, 0.1, size=(N, 16)).astype(np.float16)
+    x = g.normal(0, 1, size=K).astype(np.float16)
+    y, _, _ = oracle.lut_qgemv(codes, lut, 1, x)
+    # relabel: entry v moves to perm[v] and every code follows it
+    perm = g.permutation(16)
+    q = _unpack4(codes)
+    q2 = perm[q]
+    nib = q2.reshape(N, K // 8, 8).astype(np.uint64) << (4 * np.arange(8, dtype=np.uint64))
+    codes2 = nib.sum(axis=-1).astype(np.uint32)
+    lut2 = np.empty_like(lut)
+    lut2[:, perm] = lut
+    y2, _, _ = oracle.lut_qgemv(codes2, lut2, 1, x)
+    assert np.array_equal(y, y2)
+    # one table per 4 rows equals per-row tables that repeat it
+    shared = lut[::4]
+    ya, _, _ = oracle.lut_qgemv(codes, shared, 4, x)
+    yb, _, _ = oracle.lut_qgemv(codes, np.repeat(shared, 4, axis=0), 1, x)
+    assert np.array_equal(ya, yb)

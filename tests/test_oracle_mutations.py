@@ -34,6 +34,12 @@ MUTANTS = {
     "expert_weight_ignored": ("acc[n] += w * yd[n];", "acc[n] += yd[n];"),
     "half_truncates": ("double m = rint(ldexp(a, 10 - E));", "double m = floor(ldexp(a, 10 - E));"),
     "half_subnormal_scale": ("v = ldexp((double)mant, -24);", "v = ldexp((double)mant, -23);"),
+    "lut_one_table_per_row": ("lut + (int64_t)(n / rows_per_lut) * 16", "lut + (int64_t)n * 16"),
+    "lut_table_stride": ("lut + (int64_t)(n / rows_per_lut) * 16",
+                         "lut + (int64_t)(n / rows_per_lut) * 15"),
+    "lut_reversed_index": ("table[oracle_code(row, 4, k)]", "table[15 - oracle_code(row, 4, k)]"),
+    "lut_residual_dropped": ("            acc += r;\n", ""),
+    "lut_bound_without_x": ("mag += fabs(w) * fabs(xv);", "mag += fabs(w);"),
 }
 
 
