@@ -61,7 +61,7 @@ def parse_args():
     p.add_argument("--op", default="stack",
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, moe_routed, lm_head, lm_head_argmax, "
-                        "lm_head_sample, gemv1024, "
+                        "lm_head_sample, gemv1024, lut_layer, lut_lm_head, "
                         "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
@@ -471,7 +471,7 @@ def run_own(args):
 
 
 OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "moe_routed", "lm_head", "lm_head_argmax",
-       "lm_head_sample", "gemv1024",
+       "lm_head_sample", "gemv1024", "lut_layer", "lut_lm_head",
        "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2"]
 
 
@@ -610,6 +610,29 @@ def run_one_op(args, name):
         def call(w):
             for (key, n, k), wi in zip(shapes, w):
                 fn(wi, xs[k], y=y[:n])
+        launches = len(shapes)
+    elif name in ("lut_layer", "lut_lm_head"):
+        if name == "lut_layer":
+            config = ("LUT / palettised 4-bit (16-entry fp16 table per row): the five matvecs "
+                      "of one 8B-shaped layer")
+            shapes = [("qkv", qkv_n, H), ("o", H, H), ("gate", I, H), ("up", I, H), ("down", H, I)]
+        else:
+            config = ("LUT / palettised 4-bit, one table for the tensor: Qwen3-0.6B-shaped "
+                      "lm_head 1024->151936")
+            shapes = [("lm_head", cq["vocab"], cq["hidden"])]
+        lw = [synth.lut_weight(synth.rng(7, i, synth.TID["lut"]), n, k,
+                               1 if name == "lut_layer" else n)
+              for i, (_, n, k) in enumerate(shapes)]
+        base = tuple((torch.from_numpy(w.codes.view(np.int32)).to(dev),
+                      torch.from_numpy(w.lut).to(dev)) for w in lw)
+        rpl = [w.rows_per_lut for w in lw]
+        nbytes = sum(w.nbytes + 2 * w.K + 2 * w.N for w in lw)
+        xs = {k: torch.randn(k, device=dev).half() for _, _, k in shapes}
+        y = torch.empty(max(n for _, n, _ in shapes), device=dev).half()
+
+        def call(w):
+            for (key, n, k), wi, rows in zip(shapes, w, rpl):
+                q.qgemv_lut4(wi[0], wi[1], xs[k], rows_per_lut=rows, y=y[:n])
         launches = len(shapes)
     elif name in ("m2", "m4", "m8", "m8_w2"):
         M = int(name[1])

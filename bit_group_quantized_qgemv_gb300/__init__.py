@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     qgemv_w2g64,
     qgemv_w4g64,
     qgemv_w8g64,
+    qgemv_lut4,
     residual_rmsnorm,
     rmsnorm_qgemv,
     sample_topk,

@@ -44,6 +44,7 @@ _SIGS = {
     "qgemv_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "qgemv_residual_rmsnorm": (_I, [_P, _P, _P, _F, _I, _P, _P, _P]),
     "qgemv_sample_topk": (_I, [_P, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "qgemv_lut4": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P]),
     "qgemv_lm_head_sample": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
 }
 
@@ -258,6 +259,26 @@ def lm_head_sample(w, x, top_k, temperature, u, logits=None, token=None, want_to
                                   _ptr(token), _ptr(topk_idx), _ptr(topk_prob), _stream(stream))
     _check(st, "qgemv_lm_head_sample")
     return token, logits, topk_idx, topk_prob
+
+
+def qgemv_lut4(codes, lut, x, rows_per_lut=1, y=None, residual=None, stream=None):
+    """LUT / palettised 4-bit GEMV (qgemv_lut4): y[n] = sum_k
+    lut[n // rows_per_lut][q[n][k]] x[k] (+ residual[n]).  codes: int32/uint32
+    view [N][K/8] on the device; lut: fp16 [n_luts][16]; x: fp16 [K]."""
+    codes = _cuda(codes, _CODES, "codes")
+    lut = _cuda(lut, _F16, "lut")
+    x = _cuda(x, _F16, "x")
+    if lut.dim() != 2 or lut.shape[1] != 16:
+        raise ValueError("lut must be fp16 [n_luts][16]")
+    N, K = codes.shape[-2], codes.shape[-1] * 8
+    if y is None:
+        y = torch.empty(N, dtype=torch.float16, device=x.device)
+    _cuda(y, _F16, "y")
+    residual = _cuda(residual, _F16, "residual")
+    st = lib.qgemv_lut4(_ptr(codes), _ptr(lut), lut.shape[0], int(rows_per_lut), _ptr(x), _ptr(y),
+                        N, K, _ptr(residual), _stream(stream))
+    _check(st, "qgemv_lut4")
+    return y
 
 
 def qgemv_w8g64(w, x, y=None, residual=None, stream=None):

@@ -415,6 +415,25 @@ int qgemv_lm_head_sample(const uint32_t* codes, const uint16_t* scales, const ui
                                           static_cast<cudaStream_t>(stream)));
 }
 
+int qgemv_lut4(const uint32_t* codes, const uint16_t* lut, int n_luts, int rows_per_lut,
+               const uint16_t* x, uint16_t* y, int N, int K, const uint16_t* residual,
+               void* stream) {
+  if (!codes || !lut || !x || !y) return QGEMV_ENULL;
+  if (N < 1 || !valid_k(K) || K > QGEMV_LUT_MAX_K || rows_per_lut < 1 || n_luts < 1)
+    return QGEMV_EINVAL;
+  if (static_cast<long long>(n_luts) * rows_per_lut < N) return QGEMV_EINVAL;
+  if (!aligned(codes, 16) || !aligned(lut, 16) || !aligned(x, 16) || !aligned(y, 2) ||
+      !aligned(residual, 2))
+    return QGEMV_EALIGN;
+  int dev, sms;
+  if (int rc = current_device(&dev, &sms)) return rc;
+  return finish(qgemv::lut_qgemv_launch(codes, lut, rows_per_lut,
+                                        reinterpret_cast<const __half*>(x),
+                                        reinterpret_cast<const __half*>(residual),
+                                        reinterpret_cast<__half*>(y), N, K, sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 int qgemv_selftest_wait_timeout(unsigned limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return QGEMV_EINVAL;
   int dev = 0, sms = 0;

@@ -379,6 +379,29 @@ int qgemv_lm_head_sample(const uint32_t *codes, const uint16_t *scales, const ui
                          float temperature, const float *u, int32_t *token, int32_t *topk_idx,
                          float *topk_prob, void *stream);
 
+#define QGEMV_LUT_MAX_K 16384
+
+/*
+ * qgemv_lut4 -- the LUT / palettised 4-bit GEMV ("Boosting inference speed
+ * on Apple Silicon", INFERENCE_RESEARCH.md section 3 item 4: a LUT /
+ * palettised type, 4-bit indices and a 16-entry f16 LUT, Core ML style):
+ *   y[n] = sum_k lut[n / rows_per_lut][q[n][k]] * x[k] (+ residual[n])
+ * with fp32 accumulation and one round-to-nearest-even to fp16; every
+ * product of a table entry and an activation is exact.
+ * codes: device uint32 [N][K/8], 4-bit indices, 8 per word, low nibble
+ * first along K (the qgemv_w4g64 code layout).  lut: device fp16
+ * [n_luts][16]; table t serves rows t*rows_per_lut .. +rows_per_lut-1
+ * (rows_per_lut = N: one table for the tensor; 1: one per row).  x: fp16
+ * [K]; y: fp16 [N]; residual: fp16 [N] or NULL.  M = 1.
+ * Checks: N >= 1, K >= 64, K % 64 == 0, K <= QGEMV_LUT_MAX_K, rows_per_lut
+ * >= 1, n_luts * rows_per_lut >= N (QGEMV_EINVAL); codes, lut and x 16-byte
+ * aligned, y and residual 2-byte aligned (QGEMV_EALIGN).  One launch,
+ * chained by programmatic dependent launch.
+ */
+int qgemv_lut4(const uint32_t *codes, const uint16_t *lut, int n_luts, int rows_per_lut,
+               const uint16_t *x, uint16_t *y, int N, int K, const uint16_t *residual,
+               void *stream);
+
 /*
  * qgemv_selftest_wait_timeout -- health check of the bounded device waits
  * every kernel uses: enqueues one tiny kernel on `stream` whose thread waits

@@ -15,10 +15,12 @@ Tensor ids (the third seed word):
     10 x (activation)         11 residual        12 norm gamma (first norm)
     13 norm gamma (second)    14 MoE routing     15 spare weight
     16 MoE router weight      17 logits          18 sampling uniforms
+    19 LUT (palettised) weight
 
 Workloads (the first seed word): 0 the 1024 x 1024 GEMV, 1 the
 Llama-3.1-8B-shaped layer, 2 the Qwen3-0.6B-shaped stack, 3 the MoE, 4 the
-2-bit layer and small batches, 5 the 8-bit (Q8) layer, 6 top-k sampling.
+2-bit layer and small batches, 5 the 8-bit (Q8) layer, 6 top-k sampling,
+7 the LUT / palettised layer.
 """
 from __future__ import annotations
 
@@ -30,7 +32,7 @@ TID = {
     "qkv": 1, "o": 2, "gate": 3, "up": 4, "down": 5, "lm_head": 6,
     "moe_gu": 7, "moe_down": 8, "x": 10, "residual": 11, "gamma1": 12,
     "gamma2": 13, "routing": 14, "spare": 15, "router": 16, "logits": 17,
-    "u": 18,
+    "u": 18, "lut": 19,
 }
 
 
@@ -116,6 +118,38 @@ def routing(g: np.random.Generator, n_experts: int, top_k: int = 4,
     ex = np.exp(logits - logits.max())
     wt = (ex / ex.sum()).astype(np.float32)
     return idx, wt
+
+
+@dataclass
+class LutWeight:
+    """A LUT / palettised 4-bit weight: uint32 codes [N][K/8] (8 indices per
+    word, low nibble first) and fp16 tables [n_luts][16], table t serving
+    rows t*rows_per_lut .. +rows_per_lut-1."""
+    codes: np.ndarray
+    lut: np.ndarray
+    rows_per_lut: int
+
+    @property
+    def N(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.codes.shape[1] * 8
+
+    @property
+    def nbytes(self) -> int:
+        return self.codes.nbytes + self.lut.nbytes
+
+
+def lut_weight(g: np.random.Generator, N: int, K: int, rows_per_lut: int = 1,
+               spread: float = 0.02) -> LutWeight:
+    """Uniform random indices (uniform uint32 words) and, per table, 16
+    sorted N(0, spread) values in fp16 (the shape of a k-means palette)."""
+    codes = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    n_luts = -(-N // rows_per_lut)
+    lut = np.sort(g.normal(0.0, spread, size=(n_luts, 16)), axis=1).astype(np.float16)
+    return LutWeight(codes, lut, rows_per_lut)
 
 
 def logits(g: np.random.Generator, N: int, spread: float = 2.5, peaks: int = 8,

@@ -32,7 +32,7 @@ def test_header_lists_the_boundary():
               "decode_attention_seq1", "qgemv_device_status",
               "qgemv_selftest_wait_timeout", "qgemv_decode_stack", "qgemv_lm_head_argmax",
               "qgemv_argmax_scratch_bytes", "qgemv_moe_router", "qgemv_residual_rmsnorm",
-              "qgemv_sample_topk", "qgemv_lm_head_sample"]:
+              "qgemv_sample_topk", "qgemv_lm_head_sample", "qgemv_lut4"]:
         assert n in names
 
 
@@ -146,6 +146,23 @@ def test_sample_topk_host_checks(q):
         args[i] = two
         assert L.qgemv_sample_topk(*args, None) == -3
     assert L.qgemv_sample_topk(_fake_ptr(0x10001), 100, 5, 1.0, p, p, None, None, None) == -3
+
+
+def test_lut4_host_checks(q):
+    p, eight = _fake_ptr(), _fake_ptr(0x10008)
+    L = q.lib
+    for N, K, nl, R in ((0, 64, 1, 1), (8, 96, 8, 1), (8, 32, 8, 1), (8, 16448, 8, 1),
+                        (8, 64, 8, 0), (8, 64, 0, 8), (9, 64, 4, 2), (8, 64, 1, 7)):
+        assert L.qgemv_lut4(p, p, nl, R, p, p, N, K, None, None) == -1
+    for i in (0, 1, 4, 5):                  # codes, lut, x, y are required
+        args = [p, p, 8, 1, p, p, 8, 64, None]
+        args[i] = None
+        assert L.qgemv_lut4(*args, None) == -2
+    for i in (0, 1, 4):                     # codes, lut, x: 16 bytes
+        args = [p, p, 8, 1, p, p, 8, 64, None]
+        args[i] = eight
+        assert L.qgemv_lut4(*args, None) == -3
+    assert L.qgemv_lut4(p, p, 8, 1, p, _fake_ptr(0x10001), 8, 64, None, None) == -3
 
 
 def test_misaligned_status(q):

@@ -124,6 +124,21 @@ def test_moe_writes_only_y_and_workspace(E, H, I, top_k):
     check(y, y64, tol, f"guarded moe E={E} H={H} I={I} k={top_k}")
 
 
+@pytest.mark.parametrize("N,K,R", [(1000, 2048, 1), (301, 4096, 3), (77, 14336, 77)])
+def test_lut_writes_only_y(N, K, R):
+    w = synth.lut_weight(synth.rng(300, N + K, 19), N, K, R)
+    x = X(N + 5, K)
+    r = X(N + 6, N)
+    buf, y = guarded(N)
+    codes = torch.from_numpy(w.codes.view(np.int32)).cuda()
+    q.qgemv_lut4(codes, torch.from_numpy(w.lut).cuda(), dev16(x), rows_per_lut=R, y=y,
+                 residual=dev16(r))
+    torch.cuda.synchronize()
+    assert_guards(buf, N, f"lut N={N} K={K} R={R}")
+    y64, _, bound = oracle.lut_qgemv(w.codes, w.lut, R, x, r)
+    check(y, y64, plain_tol(bound), f"guarded lut N={N} K={K} R={R}")
+
+
 def test_attention_seq1_writes_only_out():
     n_q, n_kv, d = 6, 2, 64
     qkv = X(5, (n_q + 2 * n_kv) * d)
