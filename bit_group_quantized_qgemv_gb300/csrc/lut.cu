@@ -2,17 +2,21 @@
 // (+ residual[n]), 4-bit codes 8 per uint32 (low nibble first) indexing a
 // 16-entry fp16 table shared by R consecutive rows.
 //
-// Each warp takes RA rows at a time; lane l walks the 32-k chunks
-// c = l + 32 j of those rows (one 16-byte load of codes per chunk and row).
-// The table lookup runs in registers: a row's 16 entries become 8 byte
-// planes (low and high bytes of entries 0-7 and 8-15), and one byte permute
-// looks up 4 codes at once (their low 3 bits as the selector); a second
-// permute turns bit 3 of each code into a byte mask that picks between the
-// two halves of the table, and two more interleave the bytes into fp16
-// pairs.  The products with the fp16 activations are exact in the mixed
-// fma.rn.f32.f16 and accumulate in fp32.  x is staged in shared memory, its
-// 16-byte pieces XOR-swizzled so that the 8 lanes of each quarter-warp read
-// 8 different bank groups.
+// Each warp walks its rows (warp w of W: rows w, w + W, ...) as a stream of
+// items (row, j): lane l takes the 32-k chunk c = l + 32 j of the row, one
+// 16-byte load of codes.  The loads run D items ahead of the arithmetic
+// (a register ring unrolled by D), so every lane keeps D loads in flight
+// whatever K is.  A row's table (32 bytes) is loaded by lanes 0 and 1 with
+// the row's first item and handed to the warp by shuffles; one table for
+// the whole tensor is read once.  The lookup runs in registers: the table
+// as byte planes (low and high bytes of entries 0-7 and 8-15), one byte
+// permute per 4 codes and plane with the codes' low 3 bits as selector, a
+// permute-built byte mask from the codes' top bit to pick the half-table,
+// and two permutes interleaving the bytes into fp16 pairs.  The products
+// with the fp16 activations are exact in the mixed fma.rn.f32.f16 and
+// accumulate in fp32.  x is staged in shared memory, its 16-byte pieces
+// XOR-swizzled so that the 8 lanes of each quarter-warp read 8 different
+// bank groups.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,9 +42,8 @@ struct Planes {
   uint32_t lo_a0, lo_a1, lo_b0, lo_b1, hi_a0, hi_a1, hi_b0, hi_b1;
 };
 
-__device__ __forceinline__ Planes load_planes(const uint16_t* __restrict__ t) {
-  const uint4 p = *reinterpret_cast<const uint4*>(t);      // entries 0..7
-  const uint4 q = *reinterpret_cast<const uint4*>(t + 8);  // entries 8..15
+__device__ __forceinline__ Planes make_planes(const uint4& p, const uint4& q) {
+  // p: entries 0..7, q: entries 8..15 (fp16 pairs, low entry in the low half)
   Planes L;
   L.lo_a0 = prmt(p.x, p.y, 0x6420u);
   L.hi_a0 = prmt(p.x, p.y, 0x7531u);
@@ -53,18 +56,37 @@ __device__ __forceinline__ Planes load_planes(const uint16_t* __restrict__ t) {
   return L;
 }
 
-// The entries of the 4 codes in the low 16 bits of v as fp16 pairs
-// (e[q0], e[q1]) and (e[q2], e[q3]).
-__device__ __forceinline__ void lookup4(const Planes& L, uint32_t v, uint32_t& p01,
-                                        uint32_t& p23) {
-  const uint32_t sel = v & 0x7777u;               // low 3 bits: byte within a half-table
-  const uint32_t m = prmt(v << 4, v, 0xD9C8u);    // byte i = 0xFF when bit 3 of code i is set
-  const uint32_t la = prmt(L.lo_a0, L.lo_a1, sel), lb = prmt(L.lo_b0, L.lo_b1, sel);
-  const uint32_t ha = prmt(L.hi_a0, L.hi_a1, sel), hb = prmt(L.hi_b0, L.hi_b1, sel);
-  const uint32_t lo = (la & ~m) | (lb & m);
-  const uint32_t hi = (ha & ~m) | (hb & m);
-  p01 = prmt(lo, hi, 0x5140u);
-  p23 = prmt(lo, hi, 0x7362u);
+// The table whose halves lanes 0 (entries 0..7) and 1 (8..15) hold in v.
+__device__ __forceinline__ Planes planes_from_lanes(const uint4& v) {
+  uint4 p, q;
+  p.x = __shfl_sync(0xffffffffu, v.x, 0);
+  p.y = __shfl_sync(0xffffffffu, v.y, 0);
+  p.z = __shfl_sync(0xffffffffu, v.z, 0);
+  p.w = __shfl_sync(0xffffffffu, v.w, 0);
+  q.x = __shfl_sync(0xffffffffu, v.x, 1);
+  q.y = __shfl_sync(0xffffffffu, v.y, 1);
+  q.z = __shfl_sync(0xffffffffu, v.z, 1);
+  q.w = __shfl_sync(0xffffffffu, v.w, 1);
+  return make_planes(p, q);
+}
+
+// The entries of the 8 codes of w as fp16 pairs (e[q0], e[q1]), ...,
+// (e[q6], e[q7]).
+__device__ __forceinline__ void lookup8(const Planes& L, uint32_t w, uint32_t& p01, uint32_t& p23,
+                                        uint32_t& p45, uint32_t& p67) {
+  const uint32_t sl = w & 0x77777777u;   // low 3 bits of every code; a permute reads
+  const uint32_t sh = sl >> 16;          // the low 4 selectors of its operand
+  const uint32_t w4 = w << 4;
+  const uint32_t ml = prmt(w4, w, 0xD9C8u);  // byte i = 0xFF when bit 3 of code i is set
+  const uint32_t mh = prmt(w4, w, 0xFBEAu);  // the same for codes 4..7
+  const uint32_t ll = (prmt(L.lo_a0, L.lo_a1, sl) & ~ml) | (prmt(L.lo_b0, L.lo_b1, sl) & ml);
+  const uint32_t hl = (prmt(L.hi_a0, L.hi_a1, sl) & ~ml) | (prmt(L.hi_b0, L.hi_b1, sl) & ml);
+  const uint32_t lh = (prmt(L.lo_a0, L.lo_a1, sh) & ~mh) | (prmt(L.lo_b0, L.lo_b1, sh) & mh);
+  const uint32_t hh = (prmt(L.hi_a0, L.hi_a1, sh) & ~mh) | (prmt(L.hi_b0, L.hi_b1, sh) & mh);
+  p01 = prmt(ll, hl, 0x5140u);
+  p23 = prmt(ll, hl, 0x7362u);
+  p45 = prmt(lh, hh, 0x5140u);
+  p67 = prmt(lh, hh, 0x7362u);
 }
 
 // a += w_even * x_even, b += w_odd * x_odd over 8 weights: w and x as fp16
@@ -104,86 +126,95 @@ __device__ __forceinline__ void dot_chunk(const Planes& L, const uint4& w, const
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     uint32_t p01, p23, p45, p67;
-    lookup4(L, words[m], p01, p23);
-    lookup4(L, words[m] >> 16, p45, p67);
+    lookup8(L, words[m], p01, p23, p45, p67);
     dot8(p01, p23, p45, p67, xs[x_piece(c, m)], a, b);
   }
 }
 
-// RA rows per warp at a time; U chunks of each row per lane per step.
-template <int RA, int U>
-__global__ void __launch_bounds__(kLutThreads) lut_qgemv_kernel(
+// The item pipeline: D loads of codes in flight per lane.  SHARED: one
+// table serves every row (rows_per_lut >= N).
+template <int D, bool SHARED>
+__global__ void __launch_bounds__(kLutThreads, 3) lut_qgemv_kernel(
     const uint4* __restrict__ codes, const uint16_t* __restrict__ lut, int rows_per_lut,
     const uint4* __restrict__ x, const __half* __restrict__ residual, __half* __restrict__ y,
     int N, int K) {
   extern __shared__ __align__(16) uint4 xs[];  // K / 8 pieces, swizzled
   pdl_launch_dependents();
-  const int C = K >> 5;  // 32-k chunks per row
-  pdl_wait();            // x (and the residual) come from the previous kernel
+  const int C = K >> 5;         // 32-k chunks per row
+  const int J = (C + 31) >> 5;  // items per row
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * kLutWarps;
+  const int gw = blockIdx.x * kLutWarps + (threadIdx.x >> 5);
+  const long long rows_mine = gw < N ? (N - 1 - gw) / W + 1 : 0;
+  const long long T = rows_mine * J;  // items of this warp
+
+  uint4 bc[D], bl[D];
+  // issue position: item (ir, ij) = row gw + ir W, chunk step ij
+  long long ir = 0;
+  int ij = 0;
+  auto issue = [&](uint4& c_out, uint4& l_out) {
+    if (ir < rows_mine) {
+      const long long row = gw + ir * W;
+      const int c = lane + 32 * ij;
+      c_out = c < C ? __ldcs(codes + row * C + c) : make_uint4(0u, 0u, 0u, 0u);
+      if (!SHARED && ij == 0 && lane < 2)
+        l_out = *reinterpret_cast<const uint4*>(lut + (row / rows_per_lut) * 16 + 8 * lane);
+      if (++ij == J) {
+        ij = 0;
+        ++ir;
+      }
+    }
+  };
+  // The weights do not depend on the previous kernel: start streaming them.
+#pragma unroll
+  for (int d = 0; d < D; ++d) issue(bc[d], bl[d]);
+  Planes L{};
+  if (SHARED)
+    L = make_planes(*reinterpret_cast<const uint4*>(lut), *reinterpret_cast<const uint4*>(lut + 8));
+
+  pdl_wait();  // x (and the residual) come from the previous kernel
   for (int p = threadIdx.x; p < (K >> 3); p += kLutThreads) xs[x_piece(p >> 2, p & 3)] = x[p];
   __syncthreads();
 
-  const int lane = threadIdx.x & 31;
-  const int groups = (N + RA - 1) / RA;
-  const int stride = gridDim.x * kLutWarps;
-  for (int g = blockIdx.x * kLutWarps + (threadIdx.x >> 5); g < groups; g += stride) {
-    const int r0 = g * RA;
-    Planes L[RA];
-    float a[RA], b[RA];
+  // consume position
+  long long cr = 0;
+  int cj = 0;
+  float a = 0.f, b = 0.f;
+  for (long long t0 = 0; t0 < T; t0 += D) {
 #pragma unroll
-    for (int r = 0; r < RA; ++r) {
-      const int row = r0 + r < N ? r0 + r : N - 1;  // (a duplicate row is never stored)
-      L[r] = load_planes(lut + static_cast<long long>(row / rows_per_lut) * 16);
-      a[r] = 0.f;
-      b[r] = 0.f;
-    }
-    for (int c0 = lane; c0 < C; c0 += 32 * U) {
-      uint4 w[RA][U];
+    for (int d = 0; d < D; ++d) {
+      if (t0 + d < T) {  // uniform over the warp
+        if (!SHARED && cj == 0) L = planes_from_lanes(bl[d]);
+        const int c = lane + 32 * cj;
+        if (c < C) dot_chunk(L, bc[d], xs, c, a, b);
+        if (cj == J - 1) {
+          float s = a + b;
 #pragma unroll
-      for (int r = 0; r < RA; ++r) {
-        const int row = r0 + r < N ? r0 + r : N - 1;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int c = c0 + 32 * u;
-          w[r][u] = c < C ? __ldcs(codes + static_cast<long long>(row) * C + c)
-                          : make_uint4(0u, 0u, 0u, 0u);
+          for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (lane == 0) {
+            const long long row = gw + cr * W;
+            if (residual) s += __half2float(residual[row]);
+            y[row] = __float2half_rn(s);
+          }
+          a = 0.f;
+          b = 0.f;
+          cj = 0;
+          ++cr;
+        } else {
+          ++cj;
         }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < C) {
-#pragma unroll
-          for (int r = 0; r < RA; ++r) dot_chunk(L[r], w[r][u], xs, c, a[r], b[r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < RA; ++r) {
-      float s = a[r] + b[r];
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      const int row = r0 + r;
-      if (lane == 0 && row < N) {
-        if (residual) s += __half2float(residual[row]);
-        y[row] = __float2half_rn(s);
+        issue(bc[d], bl[d]);
       }
     }
   }
 }
 
-template <int RA, int U>
+template <int D, bool SHARED>
 cudaError_t launch(const uint32_t* codes, const uint16_t* lut, int rows_per_lut, const __half* x,
                    const __half* residual, __half* y, int N, int K, int sms, cudaStream_t st) {
-  const int smem = K * 2;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(lut_qgemv_kernel<RA, U>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
-  const long long groups = (static_cast<long long>(N) + RA - 1) / RA;
-  long long blocks = (groups + kLutWarps - 1) / kLutWarps;
-  const long long cap = static_cast<long long>(sms) * 4;
+  const int smem = K * 2;  // at most 32 KB
+  long long blocks = (static_cast<long long>(N) + kLutWarps - 1) / kLutWarps;
+  const long long cap = static_cast<long long>(sms) * 3;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
@@ -195,9 +226,9 @@ cudaError_t launch(const uint32_t* codes, const uint16_t* lut, int rows_per_lut,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lut_qgemv_kernel<RA, U>, reinterpret_cast<const uint4*>(codes),
-                            lut, rows_per_lut, reinterpret_cast<const uint4*>(x), residual, y, N,
-                            K);
+  return cudaLaunchKernelEx(&cfg, lut_qgemv_kernel<D, SHARED>,
+                            reinterpret_cast<const uint4*>(codes), lut, rows_per_lut,
+                            reinterpret_cast<const uint4*>(x), residual, y, N, K);
 }
 
 }  // namespace
@@ -205,10 +236,9 @@ cudaError_t launch(const uint32_t* codes, const uint16_t* lut, int rows_per_lut,
 cudaError_t lut_qgemv_launch(const uint32_t* codes, const uint16_t* lut, int rows_per_lut,
                              const __half* x, const __half* residual, __half* y, int N, int K,
                              int sms, cudaStream_t st) {
-  // Short rows: more rows in flight per warp; long rows: more chunks.
-  if (K <= 2048) return launch<4, 1>(codes, lut, rows_per_lut, x, residual, y, N, K, sms, st);
-  if (K <= 4096) return launch<2, 2>(codes, lut, rows_per_lut, x, residual, y, N, K, sms, st);
-  return launch<1, 4>(codes, lut, rows_per_lut, x, residual, y, N, K, sms, st);
+  if (rows_per_lut >= N)
+    return launch<4, true>(codes, lut, rows_per_lut, x, residual, y, N, K, sms, st);
+  return launch<4, false>(codes, lut, rows_per_lut, x, residual, y, N, K, sms, st);
 }
 
 }  // namespace qgemv
