@@ -132,9 +132,10 @@ __device__ __forceinline__ void dot_chunk(const Planes& L, const uint4& w, const
 }
 
 // The item pipeline: D loads of codes in flight per lane.  SHARED: one
-// table serves every row (rows_per_lut >= N).
+// table serves every row (rows_per_lut >= N); it needs fewer registers, so
+// four CTAs fit per SM instead of three.
 template <int D, bool SHARED>
-__global__ void __launch_bounds__(kLutThreads, 3) lut_qgemv_kernel(
+__global__ void __launch_bounds__(kLutThreads, SHARED ? 4 : 3) lut_qgemv_kernel(
     const uint4* __restrict__ codes, const uint16_t* __restrict__ lut, int rows_per_lut,
     const uint4* __restrict__ x, const __half* __restrict__ residual, __half* __restrict__ y,
     int N, int K) {
@@ -214,7 +215,7 @@ cudaError_t launch(const uint32_t* codes, const uint16_t* lut, int rows_per_lut,
                    const __half* residual, __half* y, int N, int K, int sms, cudaStream_t st) {
   const int smem = K * 2;  // at most 32 KB
   long long blocks = (static_cast<long long>(N) + kLutWarps - 1) / kLutWarps;
-  const long long cap = static_cast<long long>(sms) * 3;
+  const long long cap = static_cast<long long>(sms) * (SHARED ? 4 : 3);  // CTAs resident per SM
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
