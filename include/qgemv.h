@@ -39,6 +39,13 @@
  *     same pointer as `y` (an in-place residual add).
  *   - Calls are asynchronous and thread-compatible: concurrent calls on
  *     different streams are safe when their outputs do not overlap.
+ *   - Launches are chained by programmatic dependent launch: a kernel may
+ *     start while the kernel enqueued before it on `stream` is still
+ *     running and may already read its weights (codes, scales, biases,
+ *     tables, norm weights); it waits for that kernel to complete before it
+ *     reads activations, residuals, logits or u and before it writes.  So
+ *     weights must not be written by the kernel enqueued immediately
+ *     before the call on the same stream; anything earlier is ordered.
  */
 #ifndef QGEMV_H_
 #define QGEMV_H_
