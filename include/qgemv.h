@@ -43,7 +43,8 @@
  *     start while the kernel enqueued before it on `stream` is still
  *     running and may already read its weights (codes, scales, biases,
  *     tables, norm weights); it waits for that kernel to complete before it
- *     reads activations, residuals, logits or u and before it writes.  So
+ *     reads anything else (activations, residuals, expert indices and
+ *     weights, logits, u) and before it writes.  So
  *     weights must not be written by the kernel enqueued immediately
  *     before the call on the same stream; anything earlier is ordered.
  */
