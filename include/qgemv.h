@@ -367,7 +367,9 @@ size_t qgemv_argmax_scratch_bytes(void);
  * outputs (NULL to skip).  Logits are expected finite: a non-finite logit
  * still yields one of the candidates, with unspecified weights.  Checks:
  * 1 <= N <= QGEMV_SAMPLE_MAX_N, 1 <= top_k <= min(N, QGEMV_SAMPLE_MAX_K),
- * temperature finite and > 0.  One launch of a cluster of 8 CTAs (each holds
+ * temperature finite and > 0 (QGEMV_EINVAL); logits, u and token non-NULL
+ * (QGEMV_ENULL); logits 2-byte, u, token, topk_idx and topk_prob 4-byte
+ * aligned (QGEMV_EALIGN).  One launch of a cluster of 8 CTAs (each holds
  * N/8 logits in shared memory), chained to the previous kernel on `stream`
  * by programmatic dependent launch; no scratch, no allocation.
  */
