@@ -189,3 +189,27 @@ def test_lm_head_sample_parity(N, K, k):
     assert np.array_equal(idx.cpu().numpy(), cand)
     assert_token(int(tok.item()), lv, k, 0.8, u, f"lm_head_sample N={N} K={K} token")
     check_sample(lv, k, 0.8, [u], f"lm_head_sample N={N} K={K}", logits_dev=logits)
+
+
+def test_lm_head_sample_in_a_captured_graph():
+    # the GEMV and the sampler as graph nodes joined by a programmatic
+    # dependency: every replay (with a fresh u) equals the eager call
+    N, K, k = 151936, 1024, 50
+    w = synth.quant_weight(synth.rng(6, 77, synth.TID["lm_head"]), N, K, 4)
+    x = dev16(synth.activation(synth.rng(6, 78, synth.TID["x"]), K))
+    wd = dev_weight(w)
+    ud = torch.zeros(1, dtype=torch.float32, device="cuda")
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(N, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    q.lm_head_sample(wd, x, k, 0.8, ud, logits=logits, token=tok)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        q.lm_head_sample(wd, x, k, 0.8, ud, logits=logits, token=tok, stream=s)
+    for u in U(79, 16):
+        ud.fill_(float(u))
+        g.replay()
+        got = int(tok.item())
+        want, _, _, _ = q.lm_head_sample(wd, x, k, 0.8, torch.tensor([float(u)], device="cuda"))
+        assert got == int(want.item()), f"u={u}"
