@@ -382,6 +382,47 @@ def test_moe_bad_index_sets_flag_and_drops_expert():
         assert np.array_equal(y, yk)
 
 
+def _np_moe_tol(gu, dn, idx, wt, x, r):
+    """The propagated MoE tolerance, computed from dense numpy matrices built
+    through the byte-view unpack: per valid expert, the SwiGLU bound tol_h
+    of its h, then 2e-3 * (sum_k |wt_k| sum_j |Wd_nj| (|h_kj| + tol_h_kj / 2e-3)
+    + |r_n|) + 1e-5."""
+    I = gu.codes.shape[1] // 2
+    xt = x.astype(np.float64)
+    mag = np.zeros(dn.codes.shape[1])
+    for e, w in zip(idx, wt):
+        if e < 0 or e >= gu.codes.shape[0]:
+            continue
+        Wgu = np_dense(synth.QuantWeight(gu.codes[e], gu.scales[e], gu.biases[e], 4))
+        Wg, Wu = Wgu[:I], Wgu[I:]
+        g, u = Wg @ xt, Wu @ xt
+        sg = g * expit(g)
+        h = sg * u
+        dg = 2e-3 * (np.abs(Wg) @ np.abs(xt))
+        du = 2e-3 * (np.abs(Wu) @ np.abs(xt))
+        tol_h = 1.1 * np.abs(u) * dg + np.abs(sg) * du + np.abs(h) * 2.0**-11 + 1e-5
+        Wd = np_dense(synth.QuantWeight(dn.codes[e], dn.scales[e], dn.biases[e], 4))
+        mag += abs(float(w)) * (np.abs(Wd) @ (np.abs(h) + tol_h / 2e-3))
+    return 2e-3 * (mag + np.abs(r.astype(np.float64))) + 1e-5
+
+
+@pytest.mark.parametrize("idx,wt", [
+    ([0, 4, 2, 5], [0.4, 0.3, 0.2, 0.1]),
+    ([3, 1, 3, 0], [0.7, -0.45, 0.25, 0.5]),       # a negative weight and a repeated expert
+    ([2, 9, -3, 5], [0.25, 0.25, 0.25, 0.25]),     # two indices out of range
+])
+def test_moe_tolerance_brute_force(idx, wt):
+    gu, dn, x, r = _moe_small(seed=15)
+    idx = np.array(idx, np.int32)
+    wt = np.array(wt, np.float32)
+    _, _, tol, _ = _call_moe(gu, dn, idx, wt, x, r)
+    ref = _np_moe_tol(gu, dn, idx, wt, x, r)
+    assert np.allclose(tol, ref, rtol=1e-10, atol=0)
+    # without the residual the |r| term is gone: tol falls by exactly 2e-3 |r|
+    _, _, tol0, _ = _call_moe(gu, dn, idx, wt, x, np.zeros_like(r))
+    assert np.allclose(tol - tol0, 2e-3 * np.abs(r.astype(np.float64)), rtol=1e-9, atol=1e-15)
+
+
 def test_moe_duplicate_index_counts_twice():
     gu, dn, x, r = _moe_small(seed=14)
     zero = np.zeros_like(r)

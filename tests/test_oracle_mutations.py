@@ -34,6 +34,12 @@ MUTANTS = {
     "expert_weight_ignored": ("acc[n] += w * yd[n];", "acc[n] += yd[n];"),
     "half_truncates": ("double m = rint(ldexp(a, 10 - E));", "double m = floor(ldexp(a, 10 - E));"),
     "half_subnormal_scale": ("v = ldexp((double)mant, -24);", "v = ldexp((double)mant, -23);"),
+    "moe_tol_h_dropped": ("hb[j] = fabs(h[j]) + th[j] / 2e-3;", "hb[j] = fabs(h[j]);"),
+    "moe_abs_matvec_signed": ("s += fabs(weight(codes, scales, biases, bits, K, n, k)) * v[k];",
+                              "s += weight(codes, scales, biases, bits, K, n, k) * v[k];"),
+    "moe_tol_signed_weight": ("mag[n] += fabs(w) * ab[n];", "mag[n] += w * ab[n];"),
+    "moe_tol_without_residual": ("tol[n] = 2e-3 * (mag[n] + fabs(r)) + 1e-5;",
+                                 "tol[n] = 2e-3 * mag[n] + 1e-5;"),
     "lut_one_table_per_row": ("lut + (int64_t)(n / rows_per_lut) * 16", "lut + (int64_t)n * 16"),
     "lut_table_stride": ("lut + (int64_t)(n / rows_per_lut) * 16",
                          "lut + (int64_t)(n / rows_per_lut) * 15"),
