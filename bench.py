@@ -313,6 +313,15 @@ def run_own(args):
     barrier()
     ms_e2e = e0.elapsed_time(e1)
     out_ok = bool(torch.isfinite(y_host.float()).all())
+    # Per-token latency with the host waiting for each token's result before
+    # issuing the next (wall clock, host sync after every token).
+    lat = []
+    for _ in range(min(Ke, 50)):
+        t0 = time.perf_counter()
+        step_e2e()
+        stream.synchronize()
+        lat.append((time.perf_counter() - t0) * 1e6)
+    lat_us = statistics.median(lat)
 
     # ---- the same token as a CUDA graph of single-op launches
     # ---- the same token as a CUDA graph of single-op launches (+ the
@@ -455,7 +464,13 @@ def run_own(args):
             "h2d_bytes_per_step": int(x_host.numel() * 2),
             "d2h_bytes_per_step": int(y_host.numel() * 2),
             "steps": Ke,
-            "how": "per token: pinned-host H2D of x, qgemv_decode_stack, D2H of y",
+            "how": "per token: pinned-host H2D of x, qgemv_decode_stack, D2H of y; "
+                   "the tokens are queued back to back with no host sync between them, "
+                   "so this is pipelined throughput, not per-token latency",
+            "synced_us_per_token": round(lat_us, 1),
+            "synced_how": "median wall-clock time of one token (H2D, stack, D2H) with the "
+                          "host waiting for its result before the next, over %d tokens"
+                          % min(Ke, 50),
         },
         "unfused": unfused,
         "gpu_launches": K * 4 * n_layers,
@@ -794,8 +809,24 @@ def oracle_step(sample, g1, g2, x, a, act):
     oracle.qgemv(4, s["down"].codes, s["down"].scales, s["down"].biases, act, x[:s["down"].N])
 
 
+def accounting_module():
+    """The byte-accounting module, loaded by file path: importing it through
+    the package would run the package's __init__, which loads libqgemv.so,
+    and the oracle arm must not map the product library."""
+    import importlib.util
+    name = "qgemv_accounting"
+    if name in sys.modules:
+        return sys.modules[name]
+    path = os.path.join(ROOT, "bit_group_quantized_qgemv_gb300", "accounting.py")
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    sys.modules[name] = mod
+    return mod
+
+
 def sample_bytes(sample, H):
-    from bit_group_quantized_qgemv_gb300 import accounting as acc
+    acc = accounting_module()
     b = 0
     for k in ("qkv", "o", "gate", "up", "down"):
         w = sample[k]

@@ -11,9 +11,11 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it until the process exits.  In host code its name is only a
 // host-side stand-in, not a device address, so the device address is taken
-// with cudaGetSymbolAddress once per device (with that device current) and
-// then passed to the kernels like any workspace.
-#include <atomic>
+// with cudaGetSymbolAddress once per device and context (with that device
+// current) and then passed to the kernels like any workspace.
+#include <cuda.h>
+
+#include <mutex>
 
 #include "qgemv.h"
 #include "qgemv_args.h"
@@ -24,27 +26,86 @@ namespace {
 __device__ __align__(256) float g_moe_scratch[QGEMV_NOALLOC_MAX_SCRATCH];
 
 constexpr int kMaxDevices = 64;
-std::atomic<float*> g_scratch_addr[kMaxDevices];
 
-// Device address of g_moe_scratch on the current device; looked up once per
-// device.  Returns nullptr if the lookup fails.
-float* scratch_on_current_device(int* status) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *status = QGEMV_EDEVICE;
-    return nullptr;
+// Per device: the context the address was looked up in (its process-unique
+// id from cuCtxGetId; 0 = none yet) and the array's device address there.
+// A cudaDeviceReset destroys the context and unloads this library's device
+// module; the next call runs in a new context with a new id, so the address
+// is looked up again instead of reusing the old one.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;
+  float* addr = nullptr;
+};
+ScratchSlot g_slots[kMaxDevices];
+std::mutex g_slots_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime (the
+// library does not link the driver library itself).
+bool driver_ctx_fns(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
+  static CtxGetCurrentFn s_cur = nullptr;
+  static CtxGetIdFn s_id = nullptr;
+  if (s_cur == nullptr || s_id == nullptr) {
+    void* f0 = nullptr;
+    void* f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault,
+                                         &q0) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q0 != cudaDriverEntryPointSuccess || q1 != cudaDriverEntryPointSuccess || !f0 || !f1)
+      return false;
+    s_cur = reinterpret_cast<CtxGetCurrentFn>(f0);
+    s_id = reinterpret_cast<CtxGetIdFn>(f1);
   }
-  float* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p != nullptr) return p;
+  *cur = s_cur;
+  *id = s_id;
+  return true;
+}
+
+// Id of the calling thread's current context, 0 if there is none yet.
+unsigned long long current_ctx_id(CtxGetCurrentFn cur, CtxGetIdFn id) {
+  CUcontext ctx = nullptr;
+  unsigned long long v = 0;
+  if (cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (id(ctx, &v) != CUDA_SUCCESS) return 0;
+  return v;
+}
+
+// Device address of g_moe_scratch in the current context of the current
+// device.  The address is looked up (cudaGetSymbolAddress, with the device
+// current) on the first call on each device and again after that device's
+// context has changed; otherwise the cached value is returned.  Returns
+// nullptr (status QGEMV_EDEVICE) if no address can be had.
+float* scratch_on_current_device(int* status) {
+  *status = QGEMV_EDEVICE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CtxGetCurrentFn cur = nullptr;
+  CtxGetIdFn id = nullptr;
+  if (!driver_ctx_fns(&cur, &id)) return nullptr;
+  std::lock_guard<std::mutex> lock(g_slots_mu);
+  unsigned long long ctx = current_ctx_id(cur, id);
+  ScratchSlot& slot = g_slots[dev];
+  if (ctx != 0 && slot.ctx_id == ctx && slot.addr != nullptr) {
+    *status = QGEMV_OK;
+    return slot.addr;
+  }
   void* addr = nullptr;
   const cudaError_t e = cudaGetSymbolAddress(&addr, g_moe_scratch);
   if (e != cudaSuccess || addr == nullptr) {
-    *status = QGEMV_EDEVICE;
+    cudaGetLastError();
     return nullptr;
   }
-  p = static_cast<float*>(addr);
-  g_scratch_addr[dev].store(p, std::memory_order_release);
-  return p;
+  // The lookup makes the device's primary context current if no context was.
+  ctx = current_ctx_id(cur, id);
+  if (ctx == 0) return nullptr;
+  slot.ctx_id = ctx;
+  slot.addr = static_cast<float*>(addr);
+  *status = QGEMV_OK;
+  return slot.addr;
 }
 
 }  // namespace
@@ -62,7 +123,14 @@ int moe_qgemv_combine_noalloc(const uint32_t* gu_codes, const uint16_t* gu_scale
                               const float* expert_w, int top_k, const uint16_t* x,
                               const uint16_t* residual, uint16_t* y, int* err_flag,
                               void* stream) {
-  if (top_k < 1 || top_k > QGEMV_MAX_TOPK || I < 1) return QGEMV_EINVAL;
+  // Null pointers and shapes first, with the statuses of moe_qgemv_combine,
+  // then the scratch capacity; alignment is checked by moe_qgemv_combine.
+  if (!gu_codes || !gu_scales || !gu_biases || !dn_codes || !dn_scales || !dn_biases ||
+      !expert_idx || !expert_w || !x || !y)
+    return QGEMV_ENULL;
+  if (n_experts < 1 || top_k < 1 || top_k > QGEMV_MAX_TOPK || H < 64 || H % 64 != 0 || I < 64 ||
+      I % 64 != 0)
+    return QGEMV_EINVAL;
   if (static_cast<long long>(top_k) * I > QGEMV_NOALLOC_MAX_SCRATCH) return QGEMV_ESCRATCH;
   int status = QGEMV_OK;
   float* scratch = scratch_on_current_device(&status);

@@ -182,11 +182,15 @@ size_t qgemv_moe_workspace_bytes(int top_k, int I);
  * memory.  Every GPU that loads the library holds that array until the
  * process exits.  The call allocates nothing, and calls no cudaMalloc or
  * cudaFree.
- *   - top_k * I must be at most QGEMV_NOALLOC_MAX_SCRATCH, else
- *     QGEMV_ESCRATCH; other arguments and checks as moe_qgemv_combine.
+ *   - Checks, in this order: a NULL required pointer gives QGEMV_ENULL;
+ *     a bad n_experts, top_k, H or I (as moe_qgemv_combine) QGEMV_EINVAL;
+ *     top_k * I above QGEMV_NOALLOC_MAX_SCRATCH QGEMV_ESCRATCH; then the
+ *     alignment checks of moe_qgemv_combine (QGEMV_EALIGN).
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and keeps it with the
+ *     id of the device's current context; a call in another context (after
+ *     cudaDeviceReset, say) looks it up again.  Make the first call on a
+ *     device, and the first after a reset, outside any stream capture.
  *   - All calls share the array and it keeps the last call's contents.
  *     Nothing in it needs to start at zero: the first kernel writes every
  *     value the second one reads.  Calls whose work overlaps on the GPU
@@ -219,8 +223,10 @@ int decode_attention_seq1(const uint16_t *qkv, uint16_t *out, int n_q, int n_kv,
 
 /*
  * Decode stack: one token through a stack of pre-norm transformer layers'
- * quantized matvecs in one launch.  INFERENCE_RESEARCH.md section 1: encode
- * the whole layer stack at once, fused kernels, zero per-token overhead.
+ * quantized matvecs in one call: 4 kernel launches per layer, chained by
+ * programmatic dependent launch and replayed from a cached CUDA graph.
+ * INFERENCE_RESEARCH.md section 1: encode the whole layer stack at once,
+ * fused kernels, zero per-token overhead.
  * Per layer l, with 4-bit g64 weights and fp16 activations:
  *   qkv     = W_qkv . rmsnorm(x_l; attn_norm)              [(n_q+2 n_kv) hd]
  *   attn    = value heads of qkv, head h -> value head h/(n_q/n_kv)

@@ -79,3 +79,17 @@ def test_reference_arm_is_silent_on_other_ranks():
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_does_not_map_the_product_library():
+    """The oracle arm counts bytes and runs the oracle only: libqgemv.so must
+    not be loaded into its process."""
+    code = ("import sys; sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', "
+            "'--warmup', '0']; sys.path.insert(0, %r); import bench; bench.main(); "
+            "maps = open('/proc/self/maps').read(); "
+            "assert 'libqgemv' not in maps, 'libqgemv.so mapped'; "
+            "assert 'liboracle' in maps; print('ok')" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().splitlines()[-1] == "ok"

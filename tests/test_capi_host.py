@@ -165,6 +165,24 @@ def test_lut4_host_checks(q):
     assert L.qgemv_lut4(p, p, 8, 1, p, _fake_ptr(0x10001), 8, 64, None, None) == -3
 
 
+def test_noalloc_status_precedence(q):
+    """The allocation-free MoE entry point checks NULL pointers, then shapes,
+    then the scratch capacity, all before touching the device."""
+    p = _fake_ptr()
+    f = q.lib.moe_qgemv_combine_noalloc
+    big_i = (q.noalloc_max_scratch_bytes() // 4 // 4 + 64) // 64 * 64   # top_k = 4 overflows
+    # NULL with an oversized I: ENULL, not ESCRATCH
+    assert f(p, p, p, p, p, p, 8, 64, big_i, None, p, 4, p, None, p, None, None) == -2
+    assert f(p, p, p, p, p, p, 8, 64, big_i, p, p, 4, p, None, None, None, None) == -2
+    # a bad shape with an oversized I: EINVAL, not ESCRATCH
+    assert f(p, p, p, p, p, p, 8, 64, big_i + 32, p, p, 4, p, None, p, None, None) == -1
+    assert f(p, p, p, p, p, p, 0, 64, big_i, p, p, 4, p, None, p, None, None) == -1
+    assert f(p, p, p, p, p, p, 8, 96, 64, p, p, 4, p, None, p, None, None) == -1
+    assert f(p, p, p, p, p, p, 8, 64, 64, p, p, 9, p, None, p, None, None) == -1
+    # valid shapes beyond the scratch: ESCRATCH
+    assert f(p, p, p, p, p, p, 8, 64, big_i, p, p, 4, p, None, p, None, None) == -6
+
+
 def test_misaligned_status(q):
     p, odd = _fake_ptr(), _fake_ptr(0x10001)
     two = _fake_ptr(0x10002)
