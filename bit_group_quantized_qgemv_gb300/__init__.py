@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     lm_head_sample,
     argmax_scratch_bytes,
     moe_qgemv_combine,
+    moe_qgemv_combine_traced,
     moe_router,
     moe_qgemv_combine_noalloc,
     noalloc_max_scratch_bytes,

@@ -27,6 +27,8 @@ _SIGS = {
     "swiglu_qgemv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _I, _I, _P]),
     "moe_qgemv_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
                                _P, _P, _P, _P]),
+    "moe_qgemv_combine_traced": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
+                                      _P, _P, _P, _P, _I, ctypes.POINTER(_I), _P]),
     "qgemv_moe_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "moe_qgemv_combine_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P,
                                        _P, _P, _P]),
@@ -343,6 +345,34 @@ def moe_qgemv_combine(gu, dn, expert_idx, expert_w, x, residual=None, y=None, wo
     return y
 
 
+def moe_qgemv_combine_traced(gu, dn, expert_idx, expert_w, x, residual=None, trace_ctas=256,
+                             err_flag=None, stream=None):
+    """moe_qgemv_combine that also returns what each CTA of its two kernels
+    read and used: (y, trace uint32 [2][trace_ctas][top_k][4], ctas launched
+    per phase).  Trace records: idx read, weight bits read, expert used (-1:
+    skipped), weight bits used (0: skipped)."""
+    gc, gs, gb = _weight(gu, "gu")
+    dc, ds, db = _weight(dn, "dn")
+    _cuda(expert_idx, (torch.int32,), "expert_idx")
+    _cuda(expert_w, (torch.float32,), "expert_w")
+    x = _cuda(x, _F16, "x")
+    _cuda(residual, _F16, "residual")
+    E, I2, H8 = gc.shape
+    I, H = I2 // 2, H8 * 8
+    top_k = expert_idx.numel()
+    y = torch.empty(H, dtype=torch.float16, device=x.device)
+    workspace = torch.empty(top_k * I, dtype=torch.float32, device=x.device)
+    trace = torch.full((2, trace_ctas, top_k, 4), -1, dtype=torch.int32, device=x.device)
+    _cuda(err_flag, (torch.int32,), "err_flag")
+    launched = (_I * 2)(0, 0)
+    st = lib.moe_qgemv_combine_traced(_ptr(gc), _ptr(gs), _ptr(gb), _ptr(dc), _ptr(ds), _ptr(db),
+                                      E, H, I, _ptr(expert_idx), _ptr(expert_w), top_k, _ptr(x),
+                                      _ptr(residual), _ptr(y), _ptr(workspace), _ptr(err_flag),
+                                      _ptr(trace), trace_ctas, launched, _stream(stream))
+    _check(st, "moe_qgemv_combine_traced")
+    return y, trace, (int(launched[0]), int(launched[1]))
+
+
 def moe_qgemv_combine_noalloc(gu, dn, expert_idx, expert_w, x, residual=None, y=None,
                               err_flag=None, stream=None):
     """moe_qgemv_combine without a workspace: the library's fixed scratch array
@@ -422,7 +452,7 @@ def stack_layers(layers):
 
 
 def decode_stack(layers, shape: StackShape, x, y=None, workspace=None, stream=None):
-    """One token through the layer stack in one launch (qgemv_decode_stack).
+    """One token through the layer stack in one call (qgemv_decode_stack).
     `layers` is a list of layer dicts or a prebuilt stack_layers() array."""
     arr = layers if isinstance(layers, ctypes.Array) else stack_layers(layers)
     x = _cuda(x, _F16, "x")

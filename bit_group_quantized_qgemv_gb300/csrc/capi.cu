@@ -60,6 +60,13 @@ int check_sample(const uint16_t* logits, int N, int top_k, float temperature, co
   return QGEMV_OK;
 }
 
+int moe_impl(const uint32_t* gu_codes, const uint16_t* gu_scales, const uint16_t* gu_biases,
+             const uint32_t* dn_codes, const uint16_t* dn_scales, const uint16_t* dn_biases,
+             int n_experts, int H, int I, const int32_t* expert_idx, const float* expert_w,
+             int top_k, const uint16_t* x, const uint16_t* residual, uint16_t* y,
+             float* workspace, int* err_flag, uint32_t* trace, int trace_ctas,
+             int* ctas_launched, void* stream);
+
 StreamArgs blank_args() {
   StreamArgs a{};
   a.M = 1;
@@ -214,6 +221,36 @@ int moe_qgemv_combine(const uint32_t* gu_codes, const uint16_t* gu_scales,
                       int I, const int32_t* expert_idx, const float* expert_w, int top_k,
                       const uint16_t* x, const uint16_t* residual, uint16_t* y, float* workspace,
                       int* err_flag, void* stream) {
+  return moe_impl(gu_codes, gu_scales, gu_biases, dn_codes, dn_scales, dn_biases, n_experts, H, I,
+                  expert_idx, expert_w, top_k, x, residual, y, workspace, err_flag, nullptr, 0,
+                  nullptr, stream);
+}
+
+int moe_qgemv_combine_traced(const uint32_t* gu_codes, const uint16_t* gu_scales,
+                             const uint16_t* gu_biases, const uint32_t* dn_codes,
+                             const uint16_t* dn_scales, const uint16_t* dn_biases, int n_experts,
+                             int H, int I, const int32_t* expert_idx, const float* expert_w,
+                             int top_k, const uint16_t* x, const uint16_t* residual, uint16_t* y,
+                             float* workspace, int* err_flag, uint32_t* trace, int trace_ctas,
+                             int* ctas_launched, void* stream) {
+  if (!trace || !ctas_launched) return QGEMV_ENULL;
+  if (trace_ctas < 1) return QGEMV_EINVAL;
+  if (!aligned(trace, 16)) return QGEMV_EALIGN;
+  return moe_impl(gu_codes, gu_scales, gu_biases, dn_codes, dn_scales, dn_biases, n_experts, H, I,
+                  expert_idx, expert_w, top_k, x, residual, y, workspace, err_flag, trace,
+                  trace_ctas, ctas_launched, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int moe_impl(const uint32_t* gu_codes, const uint16_t* gu_scales, const uint16_t* gu_biases,
+             const uint32_t* dn_codes, const uint16_t* dn_scales, const uint16_t* dn_biases,
+             int n_experts, int H, int I, const int32_t* expert_idx, const float* expert_w,
+             int top_k, const uint16_t* x, const uint16_t* residual, uint16_t* y,
+             float* workspace, int* err_flag, uint32_t* trace, int trace_ctas,
+             int* ctas_launched, void* stream) {
   if (!gu_codes || !gu_scales || !gu_biases || !dn_codes || !dn_scales || !dn_biases ||
       !expert_idx || !expert_w || !x || !y || !workspace)
     return QGEMV_ENULL;
@@ -250,13 +287,18 @@ int moe_qgemv_combine(const uint32_t* gu_codes, const uint16_t* gu_scales,
   u.rows = static_cast<long long>(top_k) * I;
   u.rows_per_expert = I;
   u.K = H;
+  u.trace = trace;
+  u.trace_ctas = trace_ctas;
   const StreamPlan pu = qgemv::make_stream_plan(qgemv::kMoeUp, 4, H, u.rows, top_k, sms);
   cudaError_t e;
   if (pu.ok && aligned(gu_codes, 16) && aligned(gu_scales, 16) && aligned(gu_biases, 16) &&
-      aligned(x, 16))
+      aligned(x, 16)) {
+    if (ctas_launched) ctas_launched[0] = pu.grid;
     e = qgemv::stream_moe_up(pu, u, st, dev);
-  else
+  } else {
+    if (ctas_launched) ctas_launched[0] = qgemv::generic_blocks(u);
     e = qgemv::generic_launch(qgemv::kMoeUp, 4, u, st);
+  }
   if (e != cudaSuccess) return finish(e);
 
   // Phase 2: y = r + sum_k wt_k Wd[e_k] h_k.
@@ -276,14 +318,24 @@ int moe_qgemv_combine(const uint32_t* gu_codes, const uint16_t* gu_scales,
   d.n_experts = n_experts;
   d.rows = H;
   d.K = I;
+  // the down phase's records follow the up phase's
+  d.trace = trace ? trace + static_cast<size_t>(trace_ctas) * top_k * 4 : nullptr;
+  d.trace_ctas = trace_ctas;
   const StreamPlan pd = qgemv::make_stream_plan(qgemv::kMoeDown, 4, I, H, top_k, sms);
   if (pd.ok && aligned(dn_codes, 16) && aligned(dn_scales, 16) && aligned(dn_biases, 16) &&
-      aligned(workspace, 16))
+      aligned(workspace, 16)) {
+    if (ctas_launched) ctas_launched[1] = pd.grid;
     e = qgemv::stream_moe_down(pd, d, st, dev);
-  else
+  } else {
+    if (ctas_launched) ctas_launched[1] = qgemv::generic_blocks(d);
     e = qgemv::generic_launch(qgemv::kMoeDown, 4, d, st);
+  }
   return finish(e);
 }
+
+}  // namespace
+
+extern "C" {
 
 int decode_attention_seq1(const uint16_t* qkv, uint16_t* out, int n_q, int n_kv, int head_dim,
                           void* stream) {

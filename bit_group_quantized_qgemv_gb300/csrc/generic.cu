@@ -12,6 +12,7 @@ namespace qgemv {
 static __device__ unsigned g_status_generic = 0;
 
 constexpr int kGenericWarps = 8;
+static_assert(kGenericWarps == 8, "generic_blocks() in qgemv_args.h counts 8 rows per CTA");
 
 // The fp16-rounded activation value the kernels multiply by.
 template <int MODE>
@@ -39,6 +40,19 @@ __global__ void __launch_bounds__(32 * kGenericWarps) generic_kernel(const Strea
       a.err_flag != nullptr) {
     for (int k = 0; k < a.top_k; ++k)
       if (a.idx[k] < 0 || a.idx[k] >= a.n_experts) *a.err_flag = 1;
+  }
+  // Opt-in trace of the (index, weight) pairs this CTA reads (every thread
+  // reads the same words; thread 0 records them).
+  if ((MODE == kMoeUp || MODE == kMoeDown) && a.trace != nullptr && threadIdx.x == 0 &&
+      static_cast<int>(blockIdx.x) < a.trace_ctas) {
+    for (int k = 0; k < a.top_k; ++k) {
+      const int e = a.idx[k];
+      const float w = a.wt[k];
+      const bool ok = e >= 0 && e < a.n_experts;
+      reinterpret_cast<uint4*>(a.trace)[blockIdx.x * a.top_k + k] =
+          make_uint4(static_cast<unsigned>(e), __float_as_uint(w),
+                     static_cast<unsigned>(ok ? e : -1), __float_as_uint(ok ? w : 0.f));
+    }
   }
   const long long row = static_cast<long long>(blockIdx.x) * kGenericWarps + warp;
   if (row >= a.rows) return;

@@ -39,6 +39,11 @@ struct StreamArgs {
   const int* idx;           // MoE expert indices [top_k]
   const float* wt;          // MoE expert weights [top_k]
   int* err_flag;            // MoE: set to 1 on a bad index (nullable)
+  // MoE, opt-in: CTA b < trace_ctas writes, per expert slot k, what it read
+  // and used: {idx[k], bits of wt[k], expert used (-1: skipped), bits of the
+  // weight used (0 when skipped)} at trace[(b * top_k + k) * 4] (nullable).
+  unsigned* trace;
+  int trace_ctas;
   int top_k, n_experts;
   long long rows;           // output rows: N, I, top_k*I (kMoeUp) or H (kMoeDown)
   int rows_per_expert;      // kMoeUp: I
@@ -239,6 +244,8 @@ cudaError_t moe_route_launch(const __half* logits, int E, int top_k, int shared,
 // *key, and *key = 0 (programmatic dependent launch: one thread).
 cudaError_t argmax_finalize_launch(unsigned long long* key, int* token, cudaStream_t st);
 cudaError_t generic_launch(int mode, int bits, const StreamArgs& a, cudaStream_t st);
+// CTAs generic_launch starts for these arguments (8 rows each).
+inline int generic_blocks(const StreamArgs& a) { return static_cast<int>((a.rows + 7) / 8); }
 cudaError_t selftest_wait_launch(uint64_t limit_ns, cudaStream_t st);
 cudaError_t attention_seq1_launch(const __half* qkv, __half* out, int n_q, int n_kv,
                                   int head_dim, cudaStream_t st);

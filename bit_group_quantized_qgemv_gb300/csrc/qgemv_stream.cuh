@@ -332,10 +332,15 @@ __global__ void __launch_bounds__(576, 1) stream_kernel(const StreamArgs a) {
       pdl_wait();  // the expert indices and weights may come from the previous kernel
       for (int k = 0; k < a.top_k; ++k) {
         const int e = a.idx[k];
+        const float w = a.wt[k];
         const bool ok = e >= 0 && e < a.n_experts;
         s_eidx[k] = ok ? e : -1;
-        s_ewt[k] = ok ? a.wt[k] : 0.f;
+        s_ewt[k] = ok ? w : 0.f;
         if (!ok && blockIdx.x == 0 && a.err_flag != nullptr) *a.err_flag = 1;
+        if (a.trace != nullptr && static_cast<int>(blockIdx.x) < a.trace_ctas)
+          reinterpret_cast<uint4*>(a.trace)[blockIdx.x * a.top_k + k] =
+              make_uint4(static_cast<unsigned>(e), __float_as_uint(w),
+                         static_cast<unsigned>(s_eidx[k]), __float_as_uint(s_ewt[k]));
       }
     }
   }

@@ -163,6 +163,33 @@ int moe_qgemv_combine(const uint32_t *gu_codes, const uint16_t *gu_scales,
                       const uint16_t *residual, uint16_t *y, float *workspace,
                       int *err_flag, void *stream);
 
+/*
+ * moe_qgemv_combine_traced -- moe_qgemv_combine that also records, for the
+ * test suite and for debugging, which expert indices and weights each CTA
+ * of its two kernels read and used (hada.io page, "Architecture du modele":
+ * the expert indices are routing decisions and must be honoured exactly).
+ * Same arguments, results and checks as moe_qgemv_combine, plus:
+ *   trace: device, 16-byte aligned, 2 * trace_ctas * top_k * 4 uint32.
+ *     CTA b < trace_ctas of phase p (0: gate.up + SwiGLU, 1: down + combine)
+ *     writes, for each expert slot k, at trace[((p * trace_ctas + b) * top_k
+ *     + k) * 4]: the int32 expert_idx[k] it read, the fp32 bits of
+ *     expert_w[k] it read, the expert it used (-1 when the index is out of
+ *     range and the slot is skipped) and the bits of the weight it used (0
+ *     when skipped).  Records of CTAs that do not exist are left untouched.
+ *   trace_ctas >= 1 (else EINVAL); ctas_launched: HOST int[2], set to the
+ *   number of CTAs each phase launched (records exist for the first
+ *   min(ctas_launched[p], trace_ctas) of them).  NULL trace or
+ *   ctas_launched: ENULL.
+ */
+int moe_qgemv_combine_traced(const uint32_t *gu_codes, const uint16_t *gu_scales,
+                             const uint16_t *gu_biases, const uint32_t *dn_codes,
+                             const uint16_t *dn_scales, const uint16_t *dn_biases,
+                             int n_experts, int H, int I, const int32_t *expert_idx,
+                             const float *expert_w, int top_k, const uint16_t *x,
+                             const uint16_t *residual, uint16_t *y, float *workspace,
+                             int *err_flag, uint32_t *trace, int trace_ctas,
+                             int *ctas_launched, void *stream);
+
 /* Workspace bytes moe_qgemv_combine needs: top_k * I fp32 values. */
 size_t qgemv_moe_workspace_bytes(int top_k, int I);
 
