@@ -67,6 +67,14 @@ int moe_impl(const uint32_t* gu_codes, const uint16_t* gu_scales, const uint16_t
              float* workspace, int* err_flag, uint32_t* trace, int trace_ctas,
              int* ctas_launched, void* stream);
 
+// One activation row (the last pass of an odd batch): the M = 1 streaming
+// kernel when it takes the shape, else the generic kernel.
+cudaError_t launch_single_row(int bits, const StreamArgs& a, int sms, cudaStream_t st, int dev) {
+  const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, a.K, a.rows, 1, sms);
+  if (p.ok) return qgemv::stream_plain(bits, p, a, st, dev);
+  return qgemv::generic_launch(qgemv::kPlain, bits, a, st);
+}
+
 StreamArgs blank_args() {
   StreamArgs a{};
   a.M = 1;
@@ -102,8 +110,34 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
     if (p.ok && al16) return finish(qgemv::stream_plain(bits, p, a, st, dev));
     return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
   }
-  // Small batch: one pass holding all M rows when it fits, else passes of
-  // at most 4 rows (each pass streams the weights once).
+  // Small batch on the tensor cores (M >= 3): one pass holding all M rows
+  // when their activations fit in shared memory, else passes of at most 4
+  // rows (a pass of 1 or 2 rows takes the CUDA-core kernels).
+  int mp = 0, smem = 0, ns = 0;
+  if (al16 && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns))
+    return finish(qgemv::stream_batch_mma(bits, a, sms, st, dev));
+  if (al16 && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns)) {
+    for (int m0 = 0; m0 < M; m0 += 4) {
+      StreamArgs ap = a;
+      ap.M = M - m0 < 4 ? M - m0 : 4;
+      ap.x = a.x + static_cast<size_t>(m0) * K;
+      ap.y = a.y + static_cast<size_t>(m0) * N;
+      if (a.residual) ap.residual = a.residual + static_cast<size_t>(m0) * N;
+      cudaError_t e;
+      if (ap.M >= 3) {
+        e = qgemv::stream_batch_mma(bits, ap, sms, st, dev);
+      } else if (ap.M == 2) {
+        const StreamPlan pm = qgemv::make_batch_plan(bits, K, N, 2, sms);
+        e = pm.ok ? qgemv::stream_batch(bits, pm, ap, st, dev)
+                  : qgemv::generic_launch(qgemv::kPlain, bits, ap, st);
+      } else {
+        e = launch_single_row(bits, ap, sms, st, dev);
+      }
+      if (e != cudaSuccess) return finish(e);
+    }
+    return QGEMV_OK;
+  }
+  // CUDA-core small-batch kernel, then the generic kernel.
   const StreamPlan p = qgemv::make_batch_plan(bits, K, N, M, sms);
   if (al16 && p.ok) return finish(qgemv::stream_batch(bits, p, a, st, dev));
   const StreamPlan p4 = qgemv::make_batch_plan(bits, K, N, 4, sms);

@@ -231,6 +231,12 @@ cudaError_t stream_moe_down(const StreamPlan& p, const StreamArgs& a, cudaStream
                             int device);
 cudaError_t stream_batch(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                          int device);
+// Tensor-core small-batch kernel (M = 2..8 in one pass).  batch_mma_plan:
+// whether a pass of M rows fits (K a multiple of 512, the staged activations
+// within their shared-memory budget); stream_batch_mma returns
+// cudaErrorNotSupported when it does not.
+bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp, int* smem, int* ns);
+cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_t st, int device);
 cudaError_t stream_argmax(const StreamPlan& p, const StreamArgs& a, cudaStream_t st, int device);
 // Single-CTA argmax of an fp16 vector (the fallback when the streaming kernel
 // does not take the shape): token = lowest index of the largest element.

@@ -1,0 +1,570 @@
+// stream_batch_mma.cu -- small-batch GEMV on the tensor cores,
+// Y[m] = W . X[m] (+ R[m]) for M = 2..8 activation rows (INFERENCE_RESEARCH.md
+// section 1: routing by M; the weights are loaded once and applied to every
+// row of the batch).
+//
+// At M > 1 the product is a real (if thin) dense contraction: every decoded
+// weight meets M activations, and on CUDA cores the M fp32 FMAs per weight
+// bound the kernel (about 8 FMAs per weight at M = 8).  Here the codes are
+// decoded exactly as in the M = 1 kernel -- masked into fp16 subnormals
+// q * 2^-24 (one AND per two codes) -- and fed as the A operand of
+// mma.sync.m16n8k16 (f16 x f16 -> f32), 16 weight rows x 16 k per MMA, with
+// the batch's activations as the B operand (n = 8 columns: batch rows).
+// Code lanes that the masks leave scaled by 16 (4-bit) or 4, 16, 64 (2-bit)
+// meet activations pre-divided by the same power of two, so one accumulator
+// takes every class.  Per 64-k quantisation group the fp32 fragment is
+// scaled and the bias term added on the CUDA cores:
+//   acc += scale * sum(q x) + bias * sum(x)           (units of 2^-24)
+// the FMA-reordered dequantisation of the hada.io page (topic 27758),
+// factored per group as in the M = 1 kernel.
+//
+// Ring, producer and epilogue warps follow the streaming kernel.  Warp 0
+// (the producer) copies stages of 16 rows x KC k with 2-D TMA tensor copies
+// (boxes of 16 rows x 128 bytes of codes, 16 rows of scales, 16 of biases,
+// swizzled so the fragment loads of 8 rows are free of bank conflicts);
+// 8 consumer warps each take KC/8 of a stage's k; warp 1 (the epilogue) sums
+// the consumer warps' partials of a 16-row tile in a fixed order, adds the
+// residual and stores fp16.  Each CTA owns a band of whole 16-row tiles.
+// The activations are staged once per CTA in shared memory, already in
+// B-fragment order, with their per-group sums; they bound the batch a pass
+// can hold (2 * M_pad * K bytes).
+#include <cuda.h>
+
+#include "qgemv_stream.cuh"
+
+namespace qgemv {
+namespace {
+
+constexpr int kMmaWarps = 8;                 // consumer warps
+constexpr int kTileRows = 16;                // rows of one MMA tile (and one stage)
+constexpr int kXsBudget = 132 * 1024;        // activation fragments + group sums
+constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;  // two tiles of warp partials
+constexpr int kDynSmemMax = 226 * 1024;      // dynamic shared memory (static barriers beside it)
+constexpr int kAlignSlack = 1024;            // the ring starts on a 1024-byte boundary
+// Smallest batch the tensor-core kernel takes.  Measured on GB300 (graph
+// replays, o_proj 4096x4096 + down 4096x14336, 4-bit): M = 2 took 21.1 us
+// here against 17.4 us for the CUDA-core kernel, whose 2 FMAs per weight
+// are cheap; from M = 3 up the tensor cores are faster (M = 4: 22.9 against
+// 25.6 us; M = 8: 40.0 against 45.8 us).
+constexpr int kMmaMinM = 3;
+
+// Geometry of one launch (host-side plan, passed to the kernel).
+struct MmaGeom {
+  int kc;          // k per stage (divides K)
+  int ccb, csb;    // code / scale bytes of one row and stage
+  int cswz;        // swizzle mask of the scale and bias boxes (see swz)
+  int stage_bytes, ns, smem_bytes, grid, prefill, tiles;
+};
+
+// Offset of logical byte `o` of a box written by a swizzled TMA copy: the
+// 16-byte chunk index (bits 4..6) is XORed with bits 7..9, as many of them
+// as the swizzle span allows (mask 0x70: 128 B, 0x30: 64 B, 0x10: 32 B).
+__device__ __forceinline__ int swz(int o, int mask) { return o ^ ((o >> 3) & mask); }
+
+// Codes of one word as four (4-bit) or eight (2-bit) fp16-subnormal pairs
+// (see dot_word4 / dot_word2): (q0, q4), 16 (q1, q5), (q2, q6), 16 (q3, q7).
+__device__ __forceinline__ void decode_word4(uint32_t w, uint32_t (&v)[4]) {
+  v[0] = w & 0x000F000Fu;
+  v[1] = w & 0x00F000F0u;
+  const uint32_t w8 = w >> 8;
+  v[2] = w8 & 0x000F000Fu;
+  v[3] = w8 & 0x00F000F0u;
+}
+__device__ __forceinline__ void decode_word2(uint32_t w, uint32_t (&v)[8]) {
+  v[0] = w & 0x00030003u;
+  v[1] = w & 0x000C000Cu;
+  v[2] = w & 0x00300030u;
+  v[3] = w & 0x00C000C0u;
+  const uint32_t w8 = w >> 8;
+  v[4] = w8 & 0x00030003u;
+  v[5] = w8 & 0x000C000Cu;
+  v[6] = w8 & 0x00300030u;
+  v[7] = w8 & 0x00C000C0u;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2-D TMA copy of one box (x: byte column, y: row) into this CTA's shared
+// memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                        uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// fp16 pair (low half of a, low half of b) or (high of a, high of b).
+__device__ __forceinline__ uint32_t pair_lo(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x5410);
+}
+__device__ __forceinline__ uint32_t pair_hi(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x7632);
+}
+
+// Both halves times 2^-s (s = 0, 2, 4, 6), one fp16 rounding (exact unless
+// the result is subnormal).
+__device__ __forceinline__ uint32_t scale_pair(uint32_t v, int s) {
+  if (s == 0) return v;
+  const __half2 f = __float2half2_rn(s == 2 ? 0.25f : (s == 4 ? 0.0625f : 0.015625f));
+  __half2 h = *reinterpret_cast<const __half2*>(&v);
+  h = __hmul2(h, f);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// B-fragment registers of one lane (batch row m, t = lane % 4) for one
+// 64-k group, from the 16 activations x[16t .. 16t+15] of that group held as
+// 8 fp16 pairs w[j] = (x[2j], x[2j+1]).  MMA mi gets registers 2 mi, 2 mi+1.
+//  4-bit: words 2t, 2t+1 of a row (k 16t .. 16t+15); MMA mi takes word
+//         2t + mi/2, code lanes (q0,q4),(q2,q6) (mi even) or 16 (q1,q5),
+//         16 (q3,q7) (mi odd, activations / 16).
+//  2-bit: word t (k 16t .. 16t+15); MMA mi takes code class 4^mi: lanes
+//         (c_mi, c_mi+8), (c_mi+4, c_mi+12), activations / 4^mi.
+template <int BITS>
+__device__ __forceinline__ void bfrag_group(const uint32_t (&w)[8], uint32_t (&b)[8]) {
+  if (BITS == 4) {
+#pragma unroll
+    for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int k0 = 8 * (mi >> 1) + (mi & 1) + 2 * r;  // pair (k0, k0 + 4)
+        const uint32_t p = (k0 & 1) ? pair_hi(w[k0 >> 1], w[(k0 >> 1) + 2])
+                                    : pair_lo(w[k0 >> 1], w[(k0 >> 1) + 2]);
+        b[2 * mi + r] = scale_pair(p, (mi & 1) ? 4 : 0);
+      }
+  } else {
+#pragma unroll
+    for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int k0 = mi + 4 * r;  // pair (k0, k0 + 8)
+        const uint32_t p = (k0 & 1) ? pair_hi(w[k0 >> 1], w[(k0 >> 1) + 4])
+                                    : pair_lo(w[k0 >> 1], w[(k0 >> 1) + 4]);
+        b[2 * mi + r] = scale_pair(p, 2 * mi);
+      }
+  }
+}
+
+template <int BITS, int MP>
+__global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
+    batch_mma_kernel(const StreamArgs a, const MmaGeom gm,
+                     const __grid_constant__ CUtensorMap tm_codes,
+                     const __grid_constant__ CUtensorMap tm_scales,
+                     const __grid_constant__ CUtensorMap tm_biases) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t redfull_bar[2];
+  __shared__ __align__(8) uint64_t redempty_bar[2];
+  __shared__ __align__(8) uint64_t xready_bar;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const int M = a.M;
+  const int N = static_cast<int>(a.rows);
+  const int G = K / 64;
+  const int KC = gm.kc;
+  const int NC = K / KC;                 // chunks per row
+  const int GPC = KC / 64;               // groups per chunk
+  const int GPW = GPC / kMmaWarps;       // groups per consumer warp and stage
+  const int NS = gm.ns;
+  // this CTA's band of whole tiles
+  const int t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * gm.tiles / gridDim.x);
+  const int t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * gm.tiles / gridDim.x);
+  const int ntiles = t1 - t0;
+  const int nstages = ntiles * NC;
+  const int scales_off = kTileRows * gm.ccb;  // after the code boxes of a stage
+  const int biases_off = scales_off + 2048;
+
+  // shared memory: the ring (1024-byte aligned for the swizzled boxes), then
+  // B fragments [G][2][4 MP][4 u32], group sums [G][8] fp32 (x 2^-24), and
+  // two tiles of warp partials [2][W][32][4].
+  uint8_t* ring = smem_raw + ((kAlignSlack - (smem_u32(smem_raw) & (kAlignSlack - 1))) &
+                              (kAlignSlack - 1));
+  uint4* xs_frag = reinterpret_cast<uint4*>(ring + static_cast<size_t>(NS) * gm.stage_bytes);
+  float* xs_sum = reinterpret_cast<float*>(xs_frag + static_cast<size_t>(G) * 2 * 4 * MP);
+  float4* red = reinterpret_cast<float4*>(xs_sum + static_cast<size_t>(G) * 8);
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kMmaWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&redfull_bar[b]), kMmaWarps);
+      mbar_init(smem_u32(&redempty_bar[b]), 1);
+    }
+    mbar_init(smem_u32(&xready_bar), kMmaWarps);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t stage_tx =
+          static_cast<uint32_t>(kTileRows) * static_cast<uint32_t>(gm.ccb + 2 * gm.csb);
+      int slot = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int st = 0; st < nstages; ++st) {
+        const int tile = st / NC, c = st - tile * NC;
+        const int row0 = (t0 + tile) * kTileRows;
+        if (st == gm.prefill && !mbar_wait(smem_u32(&xready_bar), 0, &g_status)) break;
+        if (!mbar_wait(smem_u32(&empty_bar[slot]), phase ^ 1u, &g_status)) break;
+        const uint32_t fb = smem_u32(&full_bar[slot]);
+        const uint32_t sb = smem_u32(ring + static_cast<size_t>(slot) * gm.stage_bytes);
+        mbar_arrive_expect_tx(fb, stage_tx);  // rows past N arrive zero-filled, counted
+        for (int j = 0; j < gm.ccb / 128; ++j)
+          tma_box(sb + j * 2048, &tm_codes, c * gm.ccb + j * 128, row0, fb, pol);
+        tma_box(sb + scales_off, &tm_scales, c * gm.csb, row0, fb, pol);
+        tma_box(sb + biases_off, &tm_biases, c * gm.csb, row0, fb, pol);
+        ++issued;
+        if (++slot == NS) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      // Drain: never leave while a copy into this CTA's shared memory is in flight.
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        mbar_wait(smem_u32(&full_bar[j % NS]), (j / NS) & 1, &g_status);
+    }
+    return;
+  }
+
+  const int g = lane >> 2, t = lane & 3;
+
+  // ------------------------------------------------------------ epilogue
+  if (warp == 1) {
+    pdl_wait();  // residuals and y belong to the stream order
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int b = tile & 1;
+      if (!mbar_wait(smem_u32(&redfull_bar[b]), (tile >> 1) & 1, &g_status)) return;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float4 p = red[(b * kMmaWarps + w) * 32 + lane];
+        v[0] += p.x;
+        v[1] += p.y;
+        v[2] += p.z;
+        v[3] += p.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&redempty_bar[b]));
+      const int row0 = (t0 + tile) * kTileRows;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = row0 + g + ((i & 2) ? 8 : 0);
+        const int m = 2 * t + (i & 1);
+        if (row < N && m < M) {
+          const size_t o = static_cast<size_t>(m) * N + row;
+          float y = v[i] * kTwo24;
+          if (a.residual != nullptr) y += __half2float(a.residual[o]);
+          a.y[o] = __float2half_rn(y);
+        }
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- consumers
+  const int cw = warp - 2;  // consumer warp 0..7
+  pdl_wait();               // x may come from the previous kernel
+  // Stage the activations.  A quad of lanes (t = 0..3) takes one (batch row
+  // m, group): each lane reads its 16 activations (two 16-byte loads), forms
+  // its 8 B-fragment registers and its part of the group sum; the quad adds
+  // the four parts.  Rows m in [M, MP) are zero.  Every lane runs the same
+  // number of rounds, so the quad shuffles always have all 32 lanes.
+  {
+    // Loads of kRoundBatch rounds are issued together, so the rounds wait
+    // for one L2 round trip between them, not one each.
+    constexpr int kRoundBatch = 8;
+    const int items = MP * G * 4;
+    const int rounds = (items + 32 * kMmaWarps - 1) / (32 * kMmaWarps);
+    for (int rd0 = 0; rd0 < rounds; rd0 += kRoundBatch) {
+      uint4 raw[kRoundBatch][2];
+#pragma unroll
+      for (int i = 0; i < kRoundBatch; ++i) {
+        const int item = (rd0 + i) * 32 * kMmaWarps + cw * 32 + lane;  // item % 4 == t
+        const int mg = item >> 2;
+        const int m = mg / G, gi = mg - m * G;
+        raw[i][0] = raw[i][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (rd0 + i < rounds && item < items && m < M) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K +
+                                                            gi * 64 + 16 * t);
+          raw[i][0] = src[0];
+          raw[i][1] = src[1];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRoundBatch; ++i) {
+        if (rd0 + i >= rounds) break;  // uniform across the warp
+        const int item = (rd0 + i) * 32 * kMmaWarps + cw * 32 + lane;
+        const int mg = item >> 2;
+        const int m = mg / G, gi = mg - m * G;
+        const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
+                               raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+          part += f.x + f.y;
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        uint32_t b[8];
+        bfrag_group<BITS>(w, b);
+        if (item < items) {
+          uint4* dst = xs_frag + (static_cast<size_t>(gi) * 2) * (4 * MP) + m * 4 + t;
+          dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+          dst[4 * MP] = make_uint4(b[4], b[5], b[6], b[7]);
+          if (t == 0) xs_sum[gi * 8 + m] = part * kTwoM24;
+        }
+      }
+    }
+    for (int item = cw * 32 + lane; item < (8 - MP) * G; item += 32 * kMmaWarps) {
+      const int m = MP + item / G, gi = item % G;
+      xs_sum[gi * 8 + m] = 0.f;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&xready_bar));
+  if (!mbar_wait(smem_u32(&xready_bar), 0, &g_status)) return;
+
+  const bool bl = lane < 4 * MP;  // lanes whose batch row g holds activations
+  const int cmask = gm.cswz;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int st = 0; st < nstages; ++st) {
+    const int tile = st / NC, c = st - tile * NC;
+    if (!mbar_wait(smem_u32(&full_bar[slot]), phase, &g_status)) return;
+    const uint8_t* sb = ring + static_cast<size_t>(slot) * gm.stage_bytes;
+#pragma unroll 2
+    for (int j = 0; j < GPW; ++j) {
+      const int gl = cw * GPW + j;     // group within the chunk
+      const int gi = c * GPC + gl;     // group within the row
+      uint32_t A0[8], A8[8];           // decoded pairs of rows g and g + 8
+      if (BITS == 4) {
+        const uint8_t* box = sb + (gl >> 2) * 2048;
+        const int col = (gl & 3) * 32 + t * 8;
+        const uint2 w0 = *reinterpret_cast<const uint2*>(box + swz(g * 128 + col, 0x70));
+        const uint2 w8 = *reinterpret_cast<const uint2*>(box + swz((g + 8) * 128 + col, 0x70));
+        uint32_t v[4];
+        decode_word4(w0.x, v);
+        A0[0] = v[0];
+        A0[1] = v[2];
+        A0[2] = v[1];
+        A0[3] = v[3];
+        decode_word4(w0.y, v);
+        A0[4] = v[0];
+        A0[5] = v[2];
+        A0[6] = v[1];
+        A0[7] = v[3];
+        decode_word4(w8.x, v);
+        A8[0] = v[0];
+        A8[1] = v[2];
+        A8[2] = v[1];
+        A8[3] = v[3];
+        decode_word4(w8.y, v);
+        A8[4] = v[0];
+        A8[5] = v[2];
+        A8[6] = v[1];
+        A8[7] = v[3];
+      } else {
+        const uint8_t* box = sb + (gl >> 3) * 2048;
+        const int col = (gl & 7) * 16 + t * 4;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(box + swz(g * 128 + col, 0x70));
+        const uint32_t w8 =
+            *reinterpret_cast<const uint32_t*>(box + swz((g + 8) * 128 + col, 0x70));
+        uint32_t v[8];
+        decode_word2(w0, v);
+#pragma unroll
+        for (int mi = 0; mi < 4; ++mi) {
+          A0[2 * mi] = v[mi];
+          A0[2 * mi + 1] = v[mi + 4];
+        }
+        decode_word2(w8, v);
+#pragma unroll
+        for (int mi = 0; mi < 4; ++mi) {
+          A8[2 * mi] = v[mi];
+          A8[2 * mi + 1] = v[mi + 4];
+        }
+      }
+      uint4 bq0 = make_uint4(0u, 0u, 0u, 0u), bq1 = bq0;
+      if (bl) {
+        bq0 = xs_frag[(static_cast<size_t>(gi) * 2 + 0) * (4 * MP) + lane];
+        bq1 = xs_frag[(static_cast<size_t>(gi) * 2 + 1) * (4 * MP) + lane];
+      }
+      const uint32_t B[8] = {bq0.x, bq0.y, bq0.z, bq0.w, bq1.x, bq1.y, bq1.z, bq1.w};
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi)
+        mma16816(d, A0[2 * mi], A8[2 * mi], A0[2 * mi + 1], A8[2 * mi + 1], B[2 * mi],
+                 B[2 * mi + 1]);
+      const int s0 = swz(g * gm.csb + 2 * gl, cmask);
+      const int s8 = swz((g + 8) * gm.csb + 2 * gl, cmask);
+      const float sg = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s0));
+      const float sg8 = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s8));
+      const float bg = __half2float(*reinterpret_cast<const __half*>(sb + biases_off + s0));
+      const float bg8 = __half2float(*reinterpret_cast<const __half*>(sb + biases_off + s8));
+      const float2 xs = *reinterpret_cast<const float2*>(xs_sum + gi * 8 + 2 * t);
+      acc[0] = fmaf(sg, d[0], fmaf(bg, xs.x, acc[0]));
+      acc[1] = fmaf(sg, d[1], fmaf(bg, xs.y, acc[1]));
+      acc[2] = fmaf(sg8, d[2], fmaf(bg8, xs.x, acc[2]));
+      acc[3] = fmaf(sg8, d[3], fmaf(bg8, xs.y, acc[3]));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+    if (++slot == NS) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (c == NC - 1) {  // the tile is complete: hand its partials to the epilogue
+      const int b = tile & 1;
+      if (!mbar_wait(smem_u32(&redempty_bar[b]), ((tile >> 1) & 1) ^ 1u, &g_status)) return;
+      red[(b * kMmaWarps + cw) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&redfull_bar[b]));
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    }
+  }
+}
+
+// k per stage: the largest of 4096 (2-bit only), 2048, 1024, 512 that divides K.
+int choose_kc(int bits, int K) {
+  const int cand[4] = {4096, 2048, 1024, 512};
+  for (int kc : cand)
+    if ((bits == 2 || kc <= 2048) && K % kc == 0) return kc;
+  return 0;
+}
+
+// The driver's cuTensorMapEncodeTiled, reached through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D byte-tensor map of `rows` rows of `row_bytes` bytes, boxes of
+// box_bytes x 16 rows with the given swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, long long rows, int row_bytes, int box_bytes,
+                 CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dim[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t stride[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes),
+                             static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dim, stride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BITS, int MP>
+cudaError_t launch_mma_t(const StreamArgs& a, const MmaGeom& gm, const CUtensorMap* maps,
+                         cudaStream_t stream, int device) {
+  static unsigned done_mask = 0;
+  auto* k = batch_mma_kernel<BITS, MP>;
+  cudaError_t e = ensure_smem_attr(k, kDynSmemMax, &done_mask, device);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gm.grid));
+  cfg.blockDim = dim3(64 + 32 * kMmaWarps);
+  cfg.dynamicSmemBytes = static_cast<size_t>(gm.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, gm, maps[0], maps[1], maps[2]);
+}
+
+}  // namespace
+
+// Plan of the tensor-core small-batch kernel for M activation rows held in
+// one pass (M_pad = 2, 4 or 8 columns of the MMA's B operand); false when
+// the shape does not fit (K not a multiple of 512, or the staged
+// activations above their budget).
+bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, int* smem_out,
+                    int* ns_out) {
+  if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
+  if (K % (64 * kMmaWarps) != 0 || K < 64 * kMmaWarps) return false;
+  const int mp = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
+  const int xs_bytes = 2 * mp * K + K / 2;  // B fragments + group sums
+  if (xs_bytes > kXsBudget) return false;
+  const int kc = choose_kc(bits, K);
+  if (kc == 0) return false;
+  const int stage = kTileRows * (kc * bits / 8) + 4096;
+  const int budget = kDynSmemMax - kAlignSlack - xs_bytes - kRedBytes;
+  int ns = budget / stage;
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns < 2) return false;
+  *mp_out = mp;
+  *smem_out = kAlignSlack + ns * stage + xs_bytes + kRedBytes;
+  *ns_out = ns;
+  return true;
+}
+
+cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_t st,
+                             int device) {
+  int mp = 0, smem = 0, ns = 0;
+  if (!batch_mma_plan(bits, a.K, a.rows, a.M, sms, &mp, &smem, &ns))
+    return cudaErrorNotSupported;
+  MmaGeom gm{};
+  gm.kc = choose_kc(bits, a.K);
+  gm.ccb = gm.kc * bits / 8;
+  gm.csb = gm.kc / 32;
+  // scale / bias boxes: swizzle span equal to the row (16-byte rows: none)
+  gm.cswz = gm.csb >= 128 ? 0x70 : (gm.csb >= 64 ? 0x30 : (gm.csb >= 32 ? 0x10 : 0));
+  gm.stage_bytes = kTileRows * gm.ccb + 4096;
+  gm.ns = ns;
+  gm.smem_bytes = smem;
+  const long long tiles = (a.rows + kTileRows - 1) / kTileRows;
+  gm.tiles = static_cast<int>(tiles);
+  gm.grid = static_cast<int>(tiles < sms ? tiles : sms);
+  gm.prefill = prefill_stages(gm.stage_bytes, ns);
+  const CUtensorMapSwizzle ssw = gm.csb >= 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : gm.csb >= 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : gm.csb >= 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUtensorMap maps[3];
+  const int rcb = a.K * bits / 8, rgb = a.K / 32;
+  if (!encode_rows(&maps[0], a.codes[0], a.rows, rcb, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&maps[1], a.scales[0], a.rows, rgb, gm.csb, ssw) ||
+      !encode_rows(&maps[2], a.biases[0], a.rows, rgb, gm.csb, ssw))
+    return cudaErrorInvalidValue;
+  if (bits == 4) {
+    if (mp == 2) return launch_mma_t<4, 2>(a, gm, maps, st, device);
+    if (mp == 4) return launch_mma_t<4, 4>(a, gm, maps, st, device);
+    return launch_mma_t<4, 8>(a, gm, maps, st, device);
+  }
+  if (mp == 2) return launch_mma_t<2, 2>(a, gm, maps, st, device);
+  if (mp == 4) return launch_mma_t<2, 4>(a, gm, maps, st, device);
+  return launch_mma_t<2, 8>(a, gm, maps, st, device);
+}
+
+}  // namespace qgemv
