@@ -62,7 +62,8 @@ def parse_args():
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, moe_routed, lm_head, lm_head_argmax, "
                         "lm_head_sample, gemv1024, lut_layer, lut_lm_head, "
-                        "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, or all")
+                        "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, residual_rmsnorm, "
+                        "or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
                         "enough to exceed 3x L2; 1 keeps them resident in L2, the "
@@ -487,7 +488,7 @@ def run_own(args):
 
 OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "moe_routed", "lm_head", "lm_head_argmax",
        "lm_head_sample", "gemv1024", "lut_layer", "lut_lm_head",
-       "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2"]
+       "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2", "residual_rmsnorm"]
 
 
 def run_op(args):
@@ -664,8 +665,22 @@ def run_one_op(args, name):
         def call(w):
             for wi, xi_, yi in zip(w, xs, ys):
                 fn(wi, xi_, y=yi)
-        # M = 8 holds 16 k per thread, so K = 14336 runs as two 4-row passes
+        # at M = 8 the down projection's activations (2 * 8 * 14336 bytes) do
+        # not fit the tensor-core kernel's shared memory: two 4-row passes
         launches = 3 if M == 8 else 2
+    elif name == "residual_rmsnorm":
+        config = "residual add + RMSNorm epilogue, hidden 4096 (qgemv_residual_rmsnorm)"
+        K = H
+        base = ((torch.from_numpy(synth.activation(synth.rng(1, 0, synth.TID["x"]), K)).to(dev),
+                 torch.from_numpy(synth.activation(synth.rng(1, 0, synth.TID["residual"]), K)).to(dev),
+                 torch.from_numpy(synth.norm_gamma(synth.rng(1, 0, synth.TID["gamma1"]), K)).to(dev)),)
+        nbytes = 3 * 2 * K + 2 * 2 * K  # x, r, gamma read; h, xn written
+        hbuf = torch.empty(K, device=dev).half()
+        xnbuf = torch.empty(K, device=dev).half()
+
+        def call(w):
+            q.residual_rmsnorm(w[0][0], w[0][2], w[0][1], eps, h=hbuf, xn=xnbuf)
+        launches = 1
     elif name == "qwen_stack":
         config = "config 2: Qwen3-0.6B-shaped decode stack, 28 layers + lm_head"
         graph = False  # one qgemv_decode_stack call (+ lm_head) per token
@@ -708,6 +723,8 @@ def run_one_op(args, name):
     copies = 1 if name == "qwen_stack" else max(2, int(3 * 129e6 // max(weight_bytes, 1)) + 1)
     if name == "gemv1024":
         copies = max(copies, 512)
+    if name == "residual_rmsnorm":  # 24 KB of inputs: an L2-resident epilogue by nature
+        copies = 4
     if args.copies > 0 and name != "qwen_stack":
         copies = args.copies
     ws = [base] + [tuple(tuple(t.clone() for t in wt) for wt in base) for _ in range(copies - 1)]
