@@ -19,10 +19,12 @@
 // factored per group as in the M = 1 kernel.
 //
 // Ring, producer and epilogue warps follow the streaming kernel.  Warp 0
-// (the producer) copies stages of 16 rows x KC k with 2-D TMA tensor copies
-// (boxes of 16 rows x 128 bytes of codes, 16 rows of scales, 16 of biases,
-// swizzled so the fragment loads of 8 rows are free of bank conflicts);
-// 8 consumer warps each take KC/8 of a stage's k; warp 1 (the epilogue) sums
+// (the producer) copies stages of 16 rows x KC k with 2-D TMA tensor copies:
+// rows of at most 2 KB of codes as boxes of 16 rows x 128 bytes, swizzled so
+// the fragment loads of 8 rows are free of bank conflicts; longer rows as
+// chunks of up to 2 KB per row in one dense copy per stage (see
+// dense_layout); plus 16 rows of scales and of biases.  8 consumer warps
+// each take KC/8 of a stage's k; warp 1 (the epilogue) sums
 // the consumer warps' partials of a 16-row tile in a fixed order, adds the
 // residual and stores fp16.  Each CTA owns a band of whole 16-row tiles.
 // The activations are staged once per CTA in shared memory, already in
@@ -52,7 +54,7 @@ constexpr int kMmaMinM = 3;
 struct MmaGeom {
   int kc;          // k per stage (divides K)
   int ccb, csb;    // code / scale bytes of one row and stage
-  int cswz;        // swizzle mask of the scale and bias boxes (see swz)
+  int cswz;        // swizzle mask of the scale and bias boxes (see swz; dense: unused)
   int stage_bytes, ns, smem_bytes, grid, prefill, tiles;
 };
 
@@ -153,7 +155,7 @@ __device__ __forceinline__ void bfrag_group(const uint32_t (&w)[8], uint32_t (&b
   }
 }
 
-template <int BITS, int MP>
+template <int BITS, int MP, bool DENSE>
 __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
     batch_mma_kernel(const StreamArgs a, const MmaGeom gm,
                      const __grid_constant__ CUtensorMap tm_codes,
@@ -182,8 +184,12 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   const int t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * gm.tiles / gridDim.x);
   const int ntiles = t1 - t0;
   const int nstages = ntiles * NC;
-  const int scales_off = kTileRows * gm.ccb;  // after the code boxes of a stage
-  const int biases_off = scales_off + 2048;
+  // Stage layout.  Swizzled: code boxes of 16 rows x 128 B (2 KB each), then
+  // the scale and bias boxes at 2 KB steps (1024-byte aligned).  Dense: the
+  // codes as one [16][ccb] block, then [16][csb] scales and biases (128-byte
+  // aligned).
+  const int scales_off = kTileRows * gm.ccb;
+  const int biases_off = scales_off + (DENSE ? ((kTileRows * gm.csb + 127) & ~127) : 2048);
 
   // shared memory: the ring (1024-byte aligned for the swizzled boxes), then
   // B fragments [G][2][4 MP][4 u32], group sums [G][8] fp32 (x 2^-24), and
@@ -225,8 +231,12 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         const uint32_t fb = smem_u32(&full_bar[slot]);
         const uint32_t sb = smem_u32(ring + static_cast<size_t>(slot) * gm.stage_bytes);
         mbar_arrive_expect_tx(fb, stage_tx);  // rows past N arrive zero-filled, counted
-        for (int j = 0; j < gm.ccb / 128; ++j)
-          tma_box(sb + j * 2048, &tm_codes, c * gm.ccb + j * 128, row0, fb, pol);
+        if (DENSE) {
+          tma_box(sb, &tm_codes, c * (gm.ccb / 8), row0, fb, pol);  // 8-byte elements
+        } else {
+          for (int j = 0; j < gm.ccb / 128; ++j)
+            tma_box(sb + j * 2048, &tm_codes, c * gm.ccb + j * 128, row0, fb, pol);
+        }
         tma_box(sb + scales_off, &tm_scales, c * gm.csb, row0, fb, pol);
         tma_box(sb + biases_off, &tm_biases, c * gm.csb, row0, fb, pol);
         ++issued;
@@ -355,10 +365,19 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       const int gi = c * GPC + gl;     // group within the row
       uint32_t A0[8], A8[8];           // decoded pairs of rows g and g + 8
       if (BITS == 4) {
-        const uint8_t* box = sb + (gl >> 2) * 2048;
-        const int col = (gl & 3) * 32 + t * 8;
-        const uint2 w0 = *reinterpret_cast<const uint2*>(box + swz(g * 128 + col, 0x70));
-        const uint2 w8 = *reinterpret_cast<const uint2*>(box + swz((g + 8) * 128 + col, 0x70));
+        const uint8_t* p0;
+        const uint8_t* p8;
+        if (DENSE) {
+          p0 = sb + g * gm.ccb + gl * 32 + t * 8;
+          p8 = p0 + 8 * gm.ccb;
+        } else {
+          const uint8_t* box = sb + (gl >> 2) * 2048;
+          const int col = (gl & 3) * 32 + t * 8;
+          p0 = box + swz(g * 128 + col, 0x70);
+          p8 = box + swz((g + 8) * 128 + col, 0x70);
+        }
+        const uint2 w0 = *reinterpret_cast<const uint2*>(p0);
+        const uint2 w8 = *reinterpret_cast<const uint2*>(p8);
         uint32_t v[4];
         decode_word4(w0.x, v);
         A0[0] = v[0];
@@ -381,11 +400,19 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         A8[6] = v[1];
         A8[7] = v[3];
       } else {
-        const uint8_t* box = sb + (gl >> 3) * 2048;
-        const int col = (gl & 7) * 16 + t * 4;
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(box + swz(g * 128 + col, 0x70));
-        const uint32_t w8 =
-            *reinterpret_cast<const uint32_t*>(box + swz((g + 8) * 128 + col, 0x70));
+        const uint8_t* p0;
+        const uint8_t* p8;
+        if (DENSE) {
+          p0 = sb + g * gm.ccb + gl * 16 + t * 4;
+          p8 = p0 + 8 * gm.ccb;
+        } else {
+          const uint8_t* box = sb + (gl >> 3) * 2048;
+          const int col = (gl & 7) * 16 + t * 4;
+          p0 = box + swz(g * 128 + col, 0x70);
+          p8 = box + swz((g + 8) * 128 + col, 0x70);
+        }
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(p0);
+        const uint32_t w8 = *reinterpret_cast<const uint32_t*>(p8);
         uint32_t v[8];
         decode_word2(w0, v);
 #pragma unroll
@@ -411,8 +438,8 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       for (int mi = 0; mi < 4; ++mi)
         mma16816(d, A0[2 * mi], A8[2 * mi], A0[2 * mi + 1], A8[2 * mi + 1], B[2 * mi],
                  B[2 * mi + 1]);
-      const int s0 = swz(g * gm.csb + 2 * gl, cmask);
-      const int s8 = swz((g + 8) * gm.csb + 2 * gl, cmask);
+      const int s0 = DENSE ? g * gm.csb + 2 * gl : swz(g * gm.csb + 2 * gl, cmask);
+      const int s8 = DENSE ? (g + 8) * gm.csb + 2 * gl : swz((g + 8) * gm.csb + 2 * gl, cmask);
       const float sg = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s0));
       const float sg8 = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s8));
       const float bg = __half2float(*reinterpret_cast<const __half*>(sb + biases_off + s0));
@@ -440,12 +467,31 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   }
 }
 
-// k per stage: the largest of 4096 (2-bit only), 2048, 1024, 512 that divides K.
+// Stage layout of a shape.  A whole row fits one swizzled stage when its
+// codes are at most 2 KB and its scales 128 bytes (K <= 4096): 16 boxes of
+// 16 rows x 128 B at most, conflict-free fragment loads.  Longer rows are
+// cut into chunks of KC k (the largest multiple of 512 dividing K with
+// codes of at most 2 KB per row), each stage's codes one dense copy of up
+// to 32 KB: the copy engine streams a few large copies per stage much
+// faster than many 2 KB boxes (measured on GB300: one 1-D copy per ring
+// slot reaches ~10 / 19 / 38 / 44 GB/s per SM at 4 / 8 / 16 / 32 KB), which
+// outweighs the 4-way bank conflicts of the unswizzled rows (down
+// 4096 x 14336 at M = 4: 14.8 us dense against 16.7 us in 2 KB boxes; at
+// K = 4096 the boxes win, 6.3 against 7.4 us).
+bool dense_layout(int bits, int K) { return K * bits / 8 > 2048 || K / 32 > 128; }
+
 int choose_kc(int bits, int K) {
-  const int cand[4] = {4096, 2048, 1024, 512};
-  for (int kc : cand)
-    if ((bits == 2 || kc <= 2048) && K % kc == 0) return kc;
+  if (!dense_layout(bits, K)) return (K % 512 == 0 && K >= 512) ? K : 0;
+  for (int kc = 8 * 2048 / bits; kc >= 512; kc -= 512)
+    if (K % kc == 0) return kc;
   return 0;
+}
+
+// Bytes of one ring stage for rows of K k cut into chunks of kc.
+int stage_bytes_for(int bits, int K, int kc) {
+  const int ccb = kc * bits / 8, csb = kc / 32;
+  if (dense_layout(bits, K)) return kTileRows * ccb + 2 * ((kTileRows * csb + 127) & ~127);
+  return kTileRows * ccb + 4096;
 }
 
 // The driver's cuTensorMapEncodeTiled, reached through the runtime.
@@ -469,25 +515,29 @@ EncodeTiledFn encode_fn() {
 
 // 2-D byte-tensor map of `rows` rows of `row_bytes` bytes, boxes of
 // box_bytes x 16 rows with the given swizzle.
+// (elem8: 8-byte elements, so one box row can hold up to 2 KB.)
 bool encode_rows(CUtensorMap* m, const void* base, long long rows, int row_bytes, int box_bytes,
-                 CUtensorMapSwizzle swizzle) {
+                 CUtensorMapSwizzle swizzle, bool elem8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dim[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const int es = elem8 ? 8 : 1;
+  const cuuint64_t dim[2] = {static_cast<cuuint64_t>(row_bytes / es),
+                             static_cast<cuuint64_t>(rows)};
   const cuuint64_t stride[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes),
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / es),
                              static_cast<cuuint32_t>(kTileRows)};
   const cuuint32_t estride[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dim, stride, box,
+  return fn(m, elem8 ? CU_TENSOR_MAP_DATA_TYPE_UINT64 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dim, stride, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BITS, int MP>
+template <int BITS, int MP, bool DENSE>
 cudaError_t launch_mma_t(const StreamArgs& a, const MmaGeom& gm, const CUtensorMap* maps,
                          cudaStream_t stream, int device) {
   static unsigned done_mask = 0;
-  auto* k = batch_mma_kernel<BITS, MP>;
+  auto* k = batch_mma_kernel<BITS, MP, DENSE>;
   cudaError_t e = ensure_smem_attr(k, kDynSmemMax, &done_mask, device);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -506,19 +556,19 @@ cudaError_t launch_mma_t(const StreamArgs& a, const MmaGeom& gm, const CUtensorM
 }  // namespace
 
 // Plan of the tensor-core small-batch kernel for M activation rows held in
-// one pass (M_pad = 2, 4 or 8 columns of the MMA's B operand); false when
+// one pass (M_pad = 4 or 8 columns of the MMA's B operand); false when
 // the shape does not fit (K not a multiple of 512, or the staged
 // activations above their budget).
 bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, int* smem_out,
                     int* ns_out) {
   if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
   if (K % (64 * kMmaWarps) != 0 || K < 64 * kMmaWarps) return false;
-  const int mp = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
+  const int mp = M <= 4 ? 4 : 8;
   const int xs_bytes = 2 * mp * K + K / 2;  // B fragments + group sums
   if (xs_bytes > kXsBudget) return false;
   const int kc = choose_kc(bits, K);
   if (kc == 0) return false;
-  const int stage = kTileRows * (kc * bits / 8) + 4096;
+  const int stage = stage_bytes_for(bits, K, kc);
   const int budget = kDynSmemMax - kAlignSlack - xs_bytes - kRedBytes;
   int ns = budget / stage;
   if (ns > kMaxStages) ns = kMaxStages;
@@ -538,33 +588,41 @@ cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_
   gm.kc = choose_kc(bits, a.K);
   gm.ccb = gm.kc * bits / 8;
   gm.csb = gm.kc / 32;
-  // scale / bias boxes: swizzle span equal to the row (16-byte rows: none)
-  gm.cswz = gm.csb >= 128 ? 0x70 : (gm.csb >= 64 ? 0x30 : (gm.csb >= 32 ? 0x10 : 0));
-  gm.stage_bytes = kTileRows * gm.ccb + 4096;
+  // scale / bias boxes: a swizzle span equal to the row when the row is 32,
+  // 64 or 128 bytes, else none
+  gm.cswz = gm.csb == 128 ? 0x70 : (gm.csb == 64 ? 0x30 : (gm.csb == 32 ? 0x10 : 0));
+  gm.stage_bytes = stage_bytes_for(bits, a.K, gm.kc);
   gm.ns = ns;
   gm.smem_bytes = smem;
   const long long tiles = (a.rows + kTileRows - 1) / kTileRows;
   gm.tiles = static_cast<int>(tiles);
   gm.grid = static_cast<int>(tiles < sms ? tiles : sms);
   gm.prefill = prefill_stages(gm.stage_bytes, ns);
-  const CUtensorMapSwizzle ssw = gm.csb >= 128  ? CU_TENSOR_MAP_SWIZZLE_128B
-                                 : gm.csb >= 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                 : gm.csb >= 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const bool dense = dense_layout(bits, a.K);
+  if (dense) gm.cswz = 0;
+  const CUtensorMapSwizzle ssw = gm.cswz == 0x70   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : gm.cswz == 0x30 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                 : gm.cswz == 0x10 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                   : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUtensorMap maps[3];
   const int rcb = a.K * bits / 8, rgb = a.K / 32;
-  if (!encode_rows(&maps[0], a.codes[0], a.rows, rcb, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_rows(&maps[1], a.scales[0], a.rows, rgb, gm.csb, ssw) ||
-      !encode_rows(&maps[2], a.biases[0], a.rows, rgb, gm.csb, ssw))
-    return cudaErrorInvalidValue;
+  const bool ok_maps =
+      (dense ? encode_rows(&maps[0], a.codes[0], a.rows, rcb, gm.ccb, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           true)
+             : encode_rows(&maps[0], a.codes[0], a.rows, rcb, 128, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+      encode_rows(&maps[1], a.scales[0], a.rows, rgb, gm.csb, ssw) &&
+      encode_rows(&maps[2], a.biases[0], a.rows, rgb, gm.csb, ssw);
+  if (!ok_maps) return cudaErrorInvalidValue;
+#define QGEMV_MMA_LAUNCH(B, P)                                       \
+  return dense ? launch_mma_t<B, P, true>(a, gm, maps, st, device) \
+               : launch_mma_t<B, P, false>(a, gm, maps, st, device)
   if (bits == 4) {
-    if (mp == 2) return launch_mma_t<4, 2>(a, gm, maps, st, device);
-    if (mp == 4) return launch_mma_t<4, 4>(a, gm, maps, st, device);
-    return launch_mma_t<4, 8>(a, gm, maps, st, device);
+    if (mp == 4) QGEMV_MMA_LAUNCH(4, 4);
+    QGEMV_MMA_LAUNCH(4, 8);
   }
-  if (mp == 2) return launch_mma_t<2, 2>(a, gm, maps, st, device);
-  if (mp == 4) return launch_mma_t<2, 4>(a, gm, maps, st, device);
-  return launch_mma_t<2, 8>(a, gm, maps, st, device);
+  if (mp == 4) QGEMV_MMA_LAUNCH(2, 4);
+  QGEMV_MMA_LAUNCH(2, 8);
+#undef QGEMV_MMA_LAUNCH
 }
 
 }  // namespace qgemv
