@@ -113,10 +113,10 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
   // Small batch on the tensor cores (M >= 3): one pass holding all M rows
   // when their activations fit in shared memory, else passes of at most 4
   // rows (a pass of 1 or 2 rows takes the CUDA-core kernels).
-  int mp = 0, smem = 0, ns = 0;
-  if (al16 && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns))
+  int mp = 0, smem = 0, ns = 0, cl = 1;
+  if (al16 && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl))
     return finish(qgemv::stream_batch_mma(bits, a, sms, st, dev));
-  if (al16 && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns)) {
+  if (al16 && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns, &cl)) {
     for (int m0 = 0; m0 < M; m0 += 4) {
       StreamArgs ap = a;
       ap.M = M - m0 < 4 ? M - m0 : 4;

@@ -32,6 +32,8 @@
 // can hold (2 * M_pad * K bytes).
 #include <cuda.h>
 
+#include <mutex>
+
 #include "qgemv_stream.cuh"
 
 namespace qgemv {
@@ -40,8 +42,14 @@ namespace {
 constexpr int kMmaWarps = 8;                 // consumer warps
 constexpr int kTileRows = 16;                // rows of one MMA tile (and one stage)
 constexpr int kXsBudget = 132 * 1024;        // activation fragments + group sums
+// K is split over a cluster only when one CTA cannot hold the activations:
+// measured on GB300 (graph replays), splitting when they fit anyway was
+// slower (M = 8, 4096 x 4096: 7.9 us split in 2 against 6.3 us whole; M = 4,
+// 4096 x 14336: 15.4 against 14.9 us), while M = 8 at K = 14336, which does
+// not fit, went from two passes (29.0 us) to one split pass (16.9 us).
 constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;  // two tiles of warp partials
-constexpr int kDynSmemMax = 226 * 1024;      // dynamic shared memory (static barriers beside it)
+constexpr int kDynSmemMax = 222 * 1024;      // dynamic shared memory (static barriers and the
+                                             // cluster exchange slots beside it)
 constexpr int kAlignSlack = 1024;            // the ring starts on a 1024-byte boundary
 // Smallest batch the tensor-core kernel takes.  Measured on GB300 (graph
 // replays, o_proj 4096x4096 + down 4096x14336, 4-bit): M = 2 took 21.1 us
@@ -56,6 +64,7 @@ struct MmaGeom {
   int ccb, csb;    // code / scale bytes of one row and stage
   int cswz;        // swizzle mask of the scale and bias boxes (see swz; dense: unused)
   int stage_bytes, ns, smem_bytes, grid, prefill, tiles;
+  int cl;          // CTAs per cluster splitting K (1, 2, 4)
 };
 
 // Offset of logical byte `o` of a box written by a swizzled TMA copy: the
@@ -102,6 +111,49 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, in
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// ------------------------------------------------------------ clusters
+// Rank of this CTA in its cluster, a shared-memory address of this CTA
+// mapped to the same offset in rank `r`'s shared memory, a 16-byte store
+// there, and a release arrive on an mbarrier there (cluster scope).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t r) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(r));
+  return out;
+}
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+// Bounded wait with cluster-scope acquire (for phases completed by other
+// CTAs of the cluster); gives up after about one second like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
+        "%3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    if (ok) return true;
+    if (global_timer_ns() - t0 > 1000000000ull) {
+      atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
+  }
 }
 
 // fp16 pair (low half of a, low half of b) or (high of a, high of b).
@@ -155,7 +207,7 @@ __device__ __forceinline__ void bfrag_group(const uint32_t (&w)[8], uint32_t (&b
   }
 }
 
-template <int BITS, int MP, bool DENSE>
+template <int BITS, int MP, bool DENSE, int CL>
 __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
     batch_mma_kernel(const StreamArgs a, const MmaGeom gm,
                      const __grid_constant__ CUtensorMap tm_codes,
@@ -167,21 +219,34 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   __shared__ __align__(8) uint64_t redfull_bar[2];
   __shared__ __align__(8) uint64_t redempty_bar[2];
   __shared__ __align__(8) uint64_t xready_bar;
+  // cluster split of K (CL > 1): rank 0 collects the other ranks' tile
+  // partials (cfull) and hands the slots back (cempty, on the other ranks)
+  __shared__ __align__(8) uint64_t cfull_bar[2];
+  __shared__ __align__(8) uint64_t cempty_bar[2];
+  __shared__ __align__(16) float4 xred[CL > 1 ? 2 * CL * 32 : 1];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int K = a.K;
   const int M = a.M;
   const int N = static_cast<int>(a.rows);
-  const int G = K / 64;
+  // Cluster split of K: rank r of a cluster of CL CTAs takes k in
+  // [r K/CL, (r+1) K/CL) of the cluster's rows; the CTA's own k range is
+  // what it stages, streams and reduces.
+  const int rank = CL > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const int Kc = K / CL;
+  const int kbase = rank * Kc;
+  const int G = Kc / 64;                 // groups of this CTA's k range
   const int KC = gm.kc;
-  const int NC = K / KC;                 // chunks per row
+  const int NC = Kc / KC;                // chunks per row and CTA
   const int GPC = KC / 64;               // groups per chunk
   const int GPW = GPC / kMmaWarps;       // groups per consumer warp and stage
   const int NS = gm.ns;
-  // this CTA's band of whole tiles
-  const int t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * gm.tiles / gridDim.x);
-  const int t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * gm.tiles / gridDim.x);
+  // this cluster's band of whole tiles
+  const int ncl = static_cast<int>(gridDim.x) / CL;
+  const int cid = static_cast<int>(blockIdx.x) / CL;
+  const int t0 = static_cast<int>(static_cast<long long>(cid) * gm.tiles / ncl);
+  const int t1 = static_cast<int>(static_cast<long long>(cid + 1) * gm.tiles / ncl);
   const int ntiles = t1 - t0;
   const int nstages = ntiles * NC;
   // Stage layout.  Swizzled: code boxes of 16 rows x 128 B (2 KB each), then
@@ -211,9 +276,19 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       mbar_init(smem_u32(&redempty_bar[b]), 1);
     }
     mbar_init(smem_u32(&xready_bar), kMmaWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&cfull_bar[b]), 32 * (CL - 1 > 0 ? CL - 1 : 1));
+      mbar_init(smem_u32(&cempty_bar[b]), 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
+  if (CL > 1) {
+    // every CTA's barriers exist before any remote arrive (the CTAs of a
+    // cluster run together, and none returns before this point)
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+  }
 
   // ------------------------------------------------------------ producer
   if (warp == 0) {
@@ -231,14 +306,15 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         const uint32_t fb = smem_u32(&full_bar[slot]);
         const uint32_t sb = smem_u32(ring + static_cast<size_t>(slot) * gm.stage_bytes);
         mbar_arrive_expect_tx(fb, stage_tx);  // rows past N arrive zero-filled, counted
+        const int kb = kbase + c * KC;  // first k of the stage
         if (DENSE) {
-          tma_box(sb, &tm_codes, c * (gm.ccb / 8), row0, fb, pol);  // 8-byte elements
+          tma_box(sb, &tm_codes, kb * BITS / 64, row0, fb, pol);  // 8-byte elements
         } else {
           for (int j = 0; j < gm.ccb / 128; ++j)
-            tma_box(sb + j * 2048, &tm_codes, c * gm.ccb + j * 128, row0, fb, pol);
+            tma_box(sb + j * 2048, &tm_codes, kb * BITS / 8 + j * 128, row0, fb, pol);
         }
-        tma_box(sb + scales_off, &tm_scales, c * gm.csb, row0, fb, pol);
-        tma_box(sb + biases_off, &tm_biases, c * gm.csb, row0, fb, pol);
+        tma_box(sb + scales_off, &tm_scales, kb / 32, row0, fb, pol);
+        tma_box(sb + biases_off, &tm_biases, kb / 32, row0, fb, pol);
         ++issued;
         if (++slot == NS) {
           slot = 0;
@@ -270,6 +346,31 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&redempty_bar[b]));
+      if (CL > 1) {
+        if (rank != 0) {
+          // hand this CTA's partial of the tile to rank 0 (its slot b, once
+          // rank 0 has read the tile two back from it)
+          if (tile >= 2 &&
+              !mbar_wait_cluster(smem_u32(&cempty_bar[b]), ((tile >> 1) & 1) ^ 1u, &g_status))
+            return;
+          const uint32_t dst = map_to_rank(smem_u32(&xred[(b * CL + rank) * 32 + lane]), 0);
+          st_cluster_f4(dst, make_float4(v[0], v[1], v[2], v[3]));
+          arrive_remote(map_to_rank(smem_u32(&cfull_bar[b]), 0));
+          continue;
+        }
+        // rank 0: add the other ranks' partials, in rank order
+        if (!mbar_wait_cluster(smem_u32(&cfull_bar[b]), (tile >> 1) & 1, &g_status)) return;
+        for (int r = 1; r < CL; ++r) {
+          const float4 p = xred[(b * CL + r) * 32 + lane];
+          v[0] += p.x;
+          v[1] += p.y;
+          v[2] += p.z;
+          v[3] += p.w;
+        }
+        __syncwarp();
+        if (lane == 0 && tile + 2 < ntiles)  // the slot is reused: hand it back
+          for (int r = 1; r < CL; ++r) arrive_remote(map_to_rank(smem_u32(&cempty_bar[b]), r));
+      }
       const int row0 = (t0 + tile) * kTileRows;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -310,7 +411,7 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         raw[i][0] = raw[i][1] = make_uint4(0u, 0u, 0u, 0u);
         if (rd0 + i < rounds && item < items && m < M) {
           const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K +
-                                                            gi * 64 + 16 * t);
+                                                            kbase + gi * 64 + 16 * t);
           raw[i][0] = src[0];
           raw[i][1] = src[1];
         }
@@ -478,19 +579,23 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
 // outweighs the 4-way bank conflicts of the unswizzled rows (down
 // 4096 x 14336 at M = 4: 14.8 us dense against 16.7 us in 2 KB boxes; at
 // K = 4096 the boxes win, 6.3 against 7.4 us).
-bool dense_layout(int bits, int K) { return K * bits / 8 > 2048 || K / 32 > 128; }
+// (K: the k range of one CTA; with K split across a cluster, dense always:
+// a CTA's part of a row is then too short to fill a stage with boxes.)
+bool dense_layout(int bits, int K, int cl) {
+  return cl > 1 || K * bits / 8 > 2048 || K / 32 > 128;
+}
 
-int choose_kc(int bits, int K) {
-  if (!dense_layout(bits, K)) return (K % 512 == 0 && K >= 512) ? K : 0;
+int choose_kc(int bits, int K, int cl) {
+  if (!dense_layout(bits, K, cl)) return (K % 512 == 0 && K >= 512) ? K : 0;
   for (int kc = 8 * 2048 / bits; kc >= 512; kc -= 512)
     if (K % kc == 0) return kc;
   return 0;
 }
 
 // Bytes of one ring stage for rows of K k cut into chunks of kc.
-int stage_bytes_for(int bits, int K, int kc) {
+int stage_bytes_for(int bits, int K, int kc, int cl) {
   const int ccb = kc * bits / 8, csb = kc / 32;
-  if (dense_layout(bits, K)) return kTileRows * ccb + 2 * ((kTileRows * csb + 127) & ~127);
+  if (dense_layout(bits, K, cl)) return kTileRows * ccb + 2 * ((kTileRows * csb + 127) & ~127);
   return kTileRows * ccb + 4096;
 }
 
@@ -533,23 +638,67 @@ bool encode_rows(CUtensorMap* m, const void* base, long long rows, int row_bytes
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BITS, int MP, bool DENSE>
-cudaError_t launch_mma_t(const StreamArgs& a, const MmaGeom& gm, const CUtensorMap* maps,
+// Clusters of `cl` CTAs of this kernel that can be resident at once, for a
+// shared-memory size (cudaOccupancyMaxActiveClusters, cached per device).
+template <typename F>
+int resident_clusters(F* k, int cl, int smem, int device) {
+  static std::mutex mu;
+  static int dev_of[8] = {-1, -1, -1, -1, -1, -1, -1, -1}, smem_of[8], val_of[8];
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 8; ++i)
+    if (dev_of[i] == device && smem_of[i] == smem) return val_of[i];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cl));
+  cfg.blockDim = dim3(64 + 32 * kMmaWarps);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  dev_of[next] = device;
+  smem_of[next] = smem;
+  val_of[next] = n;
+  next = (next + 1) % 8;
+  return n;
+}
+
+template <int BITS, int MP, bool DENSE, int CL>
+cudaError_t launch_mma_t(const StreamArgs& a, MmaGeom gm, const CUtensorMap* maps,
                          cudaStream_t stream, int device) {
   static unsigned done_mask = 0;
-  auto* k = batch_mma_kernel<BITS, MP, DENSE>;
+  auto* k = batch_mma_kernel<BITS, MP, DENSE, CL>;
   cudaError_t e = ensure_smem_attr(k, kDynSmemMax, &done_mask, device);
   if (e != cudaSuccess) return e;
+  int clusters = gm.grid;  // one CTA per SM and cluster rank
+  if (CL > 1) {
+    const int n = resident_clusters(k, CL, gm.smem_bytes, device);
+    if (n < 1) return cudaErrorNotSupported;
+    clusters = gm.tiles < n ? gm.tiles : n;
+  }
+  gm.grid = clusters * CL;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gm.grid));
   cfg.blockDim = dim3(64 + 32 * kMmaWarps);
   cfg.dynamicSmemBytes = static_cast<size_t>(gm.smem_bytes);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(CL);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, a, gm, maps[0], maps[1], maps[2]);
 }
 
@@ -560,15 +709,21 @@ cudaError_t launch_mma_t(const StreamArgs& a, const MmaGeom& gm, const CUtensorM
 // the shape does not fit (K not a multiple of 512, or the staged
 // activations above their budget).
 bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, int* smem_out,
-                    int* ns_out) {
+                    int* ns_out, int* cl_out) {
   if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
-  if (K % (64 * kMmaWarps) != 0 || K < 64 * kMmaWarps) return false;
   const int mp = M <= 4 ? 4 : 8;
-  const int xs_bytes = 2 * mp * K + K / 2;  // B fragments + group sums
+  // Split K across a cluster (2, then 4 CTAs) while one CTA cannot hold
+  // the staged activations.
+  auto xs_of = [&](int c) { return 2 * mp * (K / c) + (K / c) / 2; };  // fragments + group sums
+  int cl = 1;
+  while (cl < 4 && xs_of(cl) > kXsBudget && K % (2 * cl * 64 * kMmaWarps) == 0) cl *= 2;
+  const int Kc = K / cl;
+  if (Kc % (64 * kMmaWarps) != 0 || Kc < 64 * kMmaWarps) return false;
+  const int xs_bytes = xs_of(cl);
   if (xs_bytes > kXsBudget) return false;
-  const int kc = choose_kc(bits, K);
+  const int kc = choose_kc(bits, Kc, cl);
   if (kc == 0) return false;
-  const int stage = stage_bytes_for(bits, K, kc);
+  const int stage = stage_bytes_for(bits, Kc, kc, cl);
   const int budget = kDynSmemMax - kAlignSlack - xs_bytes - kRedBytes;
   int ns = budget / stage;
   if (ns > kMaxStages) ns = kMaxStages;
@@ -576,29 +731,32 @@ bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, i
   *mp_out = mp;
   *smem_out = kAlignSlack + ns * stage + xs_bytes + kRedBytes;
   *ns_out = ns;
+  *cl_out = cl;
   return true;
 }
 
 cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_t st,
                              int device) {
-  int mp = 0, smem = 0, ns = 0;
-  if (!batch_mma_plan(bits, a.K, a.rows, a.M, sms, &mp, &smem, &ns))
+  int mp = 0, smem = 0, ns = 0, cl = 1;
+  if (!batch_mma_plan(bits, a.K, a.rows, a.M, sms, &mp, &smem, &ns, &cl))
     return cudaErrorNotSupported;
   MmaGeom gm{};
-  gm.kc = choose_kc(bits, a.K);
+  gm.cl = cl;
+  const int Kc = a.K / cl;
+  gm.kc = choose_kc(bits, Kc, cl);
   gm.ccb = gm.kc * bits / 8;
   gm.csb = gm.kc / 32;
   // scale / bias boxes: a swizzle span equal to the row when the row is 32,
   // 64 or 128 bytes, else none
   gm.cswz = gm.csb == 128 ? 0x70 : (gm.csb == 64 ? 0x30 : (gm.csb == 32 ? 0x10 : 0));
-  gm.stage_bytes = stage_bytes_for(bits, a.K, gm.kc);
+  gm.stage_bytes = stage_bytes_for(bits, Kc, gm.kc, cl);
   gm.ns = ns;
   gm.smem_bytes = smem;
   const long long tiles = (a.rows + kTileRows - 1) / kTileRows;
   gm.tiles = static_cast<int>(tiles);
   gm.grid = static_cast<int>(tiles < sms ? tiles : sms);
   gm.prefill = prefill_stages(gm.stage_bytes, ns);
-  const bool dense = dense_layout(bits, a.K);
+  const bool dense = dense_layout(bits, Kc, cl);
   if (dense) gm.cswz = 0;
   const CUtensorMapSwizzle ssw = gm.cswz == 0x70   ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : gm.cswz == 0x30 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -613,9 +771,11 @@ cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_
       encode_rows(&maps[1], a.scales[0], a.rows, rgb, gm.csb, ssw) &&
       encode_rows(&maps[2], a.biases[0], a.rows, rgb, gm.csb, ssw);
   if (!ok_maps) return cudaErrorInvalidValue;
-#define QGEMV_MMA_LAUNCH(B, P)                                       \
-  return dense ? launch_mma_t<B, P, true>(a, gm, maps, st, device) \
-               : launch_mma_t<B, P, false>(a, gm, maps, st, device)
+#define QGEMV_MMA_LAUNCH(B, P)                                                  \
+  return !dense     ? launch_mma_t<B, P, false, 1>(a, gm, maps, st, device)  \
+         : cl == 1  ? launch_mma_t<B, P, true, 1>(a, gm, maps, st, device)   \
+         : cl == 2  ? launch_mma_t<B, P, true, 2>(a, gm, maps, st, device)   \
+                    : launch_mma_t<B, P, true, 4>(a, gm, maps, st, device)
   if (bits == 4) {
     if (mp == 4) QGEMV_MMA_LAUNCH(4, 4);
     QGEMV_MMA_LAUNCH(4, 8);
