@@ -19,17 +19,18 @@
 // factored per group as in the M = 1 kernel.
 //
 // Ring, producer and epilogue warps follow the streaming kernel.  Warp 0
-// (the producer) copies stages of 16 rows x KC k with 2-D TMA tensor copies:
-// rows of at most 2 KB of codes as boxes of 16 rows x 128 bytes, swizzled so
-// the fragment loads of 8 rows are free of bank conflicts; longer rows as
-// chunks of up to 2 KB per row in one dense copy per stage (see
-// dense_layout); plus 16 rows of scales and of biases.  8 consumer warps
-// each take KC/8 of a stage's k; warp 1 (the epilogue) sums
-// the consumer warps' partials of a 16-row tile in a fixed order, adds the
-// residual and stores fp16.  Each CTA owns a band of whole 16-row tiles.
-// The activations are staged once per CTA in shared memory, already in
-// B-fragment order, with their per-group sums; they bound the batch a pass
-// can hold (2 * M_pad * K bytes).
+// (the producer) copies stages of 16 rows x KC k with TMA tensor copies:
+// the codes in one 3-D copy that views each row as 128-byte columns and
+// lands them 128-byte swizzled, [column][16 rows][128 B], so the fragment
+// loads of 8 rows are free of bank conflicts; plus 16 rows of scales and of
+// biases (see chunked_layout).  8 consumer warps each take KC/8 of a stage's
+// k; warp 1 (the epilogue) sums the consumer warps' partials of a 16-row
+// tile in a fixed order, adds the residual and stores fp16.  Each CTA owns a
+// band of whole 16-row tiles.  The activations are staged in shared memory,
+// already in B-fragment order, with their per-group sums, by the consumer
+// warps themselves (each stages the groups it will read, the first chunk
+// before any math and chunk c + 1 around stage c of the first tile); they
+// bound the batch a pass can hold (2 * M_pad * K bytes).
 #include <cuda.h>
 
 #include <mutex>
@@ -48,8 +49,16 @@ constexpr int kXsBudget = 132 * 1024;        // activation fragments + group sum
 // 4096 x 14336: 15.4 against 14.9 us), while M = 8 at K = 14336, which does
 // not fit, went from two passes (29.0 us) to one split pass (16.9 us).
 constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;  // two tiles of warp partials
-constexpr int kDynSmemMax = 222 * 1024;      // dynamic shared memory (static barriers and the
-                                             // cluster exchange slots beside it)
+constexpr int kSmemPerBlock = 227 * 1024;    // sm_100-family opt-in shared memory per block
+// Dynamic shared memory of a CTA in a cluster of cl: what the block may
+// hold less a bound on the kernel's static part (barriers, 384 bytes, and
+// for cl > 1 the cluster exchange slots, 1 KB per rank).  Every byte counts:
+// for M = 4 at K = 14336 the staged activations take 119 KB, and what is
+// left holds a third 32 KB stage only at the full limit (measured on GB300,
+// down 4096 x 14336: two stages 15.3 us).
+constexpr int dyn_smem_max(int cl) { return kSmemPerBlock - 512 - (cl > 1 ? 1024 * cl : 0); }
+// Threads of a CTA: producer warp, epilogue warp, the consumer warps.
+constexpr int kBlockThreads = 64 + 32 * kMmaWarps;
 constexpr int kAlignSlack = 1024;            // the ring starts on a 1024-byte boundary
 // Smallest batch the tensor-core kernel takes.  Measured on GB300 (graph
 // replays, o_proj 4096x4096 + down 4096x14336, 4-bit): M = 2 took 21.1 us
@@ -62,7 +71,7 @@ constexpr int kMmaMinM = 3;
 struct MmaGeom {
   int kc;          // k per stage (divides K)
   int ccb, csb;    // code / scale bytes of one row and stage
-  int cswz;        // swizzle mask of the scale and bias boxes (see swz; dense: unused)
+  int cswz;        // swizzle mask of the scale and bias boxes (see swz; chunked: unused)
   int stage_bytes, ns, smem_bytes, grid, prefill, tiles;
   int cl;          // CTAs per cluster splitting K (1, 2, 4)
 };
@@ -104,6 +113,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 // 2-D TMA copy of one box (x: byte column, y: row) into this CTA's shared
 // memory, completion counted on `bar`.
+// A 3-D box {x, y, z} of a tensor map into shared memory.
+__device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y,
                                         uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -207,8 +226,8 @@ __device__ __forceinline__ void bfrag_group(const uint32_t (&w)[8], uint32_t (&b
   }
 }
 
-template <int BITS, int MP, bool DENSE, int CL>
-__global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
+template <int BITS, int MP, bool CHUNKED, int CL>
+__global__ void __launch_bounds__(kBlockThreads, 1)
     batch_mma_kernel(const StreamArgs a, const MmaGeom gm,
                      const __grid_constant__ CUtensorMap tm_codes,
                      const __grid_constant__ CUtensorMap tm_scales,
@@ -249,12 +268,12 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   const int t1 = static_cast<int>(static_cast<long long>(cid + 1) * gm.tiles / ncl);
   const int ntiles = t1 - t0;
   const int nstages = ntiles * NC;
-  // Stage layout.  Swizzled: code boxes of 16 rows x 128 B (2 KB each), then
-  // the scale and bias boxes at 2 KB steps (1024-byte aligned).  Dense: the
-  // codes as one [16][ccb] block, then [16][csb] scales and biases (128-byte
-  // aligned).
+  // Stage layout: the codes as [ccb / 128][16 rows][128 B], 128-byte
+  // swizzled (2 KB per column, 1024-byte aligned), then the scales and the
+  // biases: whole rows as swizzled boxes at 2 KB steps, chunks as plain
+  // [16][csb] blocks (128-byte aligned).
   const int scales_off = kTileRows * gm.ccb;
-  const int biases_off = scales_off + (DENSE ? ((kTileRows * gm.csb + 127) & ~127) : 2048);
+  const int biases_off = scales_off + (CHUNKED ? ((kTileRows * gm.csb + 127) & ~127) : 2048);
 
   // shared memory: the ring (1024-byte aligned for the swizzled boxes), then
   // B fragments [G][2][4 MP][4 u32], group sums [G][8] fp32 (x 2^-24), and
@@ -307,12 +326,8 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         const uint32_t sb = smem_u32(ring + static_cast<size_t>(slot) * gm.stage_bytes);
         mbar_arrive_expect_tx(fb, stage_tx);  // rows past N arrive zero-filled, counted
         const int kb = kbase + c * KC;  // first k of the stage
-        if (DENSE) {
-          tma_box(sb, &tm_codes, kb * BITS / 64, row0, fb, pol);  // 8-byte elements
-        } else {
-          for (int j = 0; j < gm.ccb / 128; ++j)
-            tma_box(sb + j * 2048, &tm_codes, kb * BITS / 8 + j * 128, row0, fb, pol);
-        }
+        // all of the stage's codes in one copy: 128-byte columns j of 16 rows
+        tma_box3(sb, &tm_codes, 0, row0, kb * BITS / 8 / 128, fb, pol);
         tma_box(sb + scales_off, &tm_scales, kb / 32, row0, fb, pol);
         tma_box(sb + biases_off, &tm_biases, kb / 32, row0, fb, pol);
         ++issued;
@@ -329,6 +344,23 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   }
 
   const int g = lane >> 2, t = lane & 3;
+
+  // Final values of a tile (lane: rows g, g + 8; batch rows 2t, 2t + 1),
+  // scaled back from 2^-24, plus the residual, rounded to fp16 into y.
+  auto store_tile = [&](int tile, const float (&v)[4]) {
+    const int row0 = (t0 + tile) * kTileRows;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = row0 + g + ((i & 2) ? 8 : 0);
+      const int m = 2 * t + (i & 1);
+      if (row < N && m < M) {
+        const size_t o = static_cast<size_t>(m) * N + row;
+        float y = v[i] * kTwo24;
+        if (a.residual != nullptr) y += __half2float(a.residual[o]);
+        a.y[o] = __float2half_rn(y);
+      }
+    }
+  };
 
   // ------------------------------------------------------------ epilogue
   if (warp == 1) {
@@ -371,18 +403,7 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         if (lane == 0 && tile + 2 < ntiles)  // the slot is reused: hand it back
           for (int r = 1; r < CL; ++r) arrive_remote(map_to_rank(smem_u32(&cempty_bar[b]), r));
       }
-      const int row0 = (t0 + tile) * kTileRows;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = row0 + g + ((i & 2) ? 8 : 0);
-        const int m = 2 * t + (i & 1);
-        if (row < N && m < M) {
-          const size_t o = static_cast<size_t>(m) * N + row;
-          float y = v[i] * kTwo24;
-          if (a.residual != nullptr) y += __half2float(a.residual[o]);
-          a.y[o] = __float2half_rn(y);
-        }
-      }
+      store_tile(tile, v);
     }
     return;
   }
@@ -390,66 +411,72 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   // ----------------------------------------------------------- consumers
   const int cw = warp - 2;  // consumer warp 0..7
   pdl_wait();               // x may come from the previous kernel
-  // Stage the activations.  A quad of lanes (t = 0..3) takes one (batch row
-  // m, group): each lane reads its 16 activations (two 16-byte loads), forms
-  // its 8 B-fragment registers and its part of the group sum; the quad adds
-  // the four parts.  Rows m in [M, MP) are zero.  Every lane runs the same
-  // number of rounds, so the quad shuffles always have all 32 lanes.
-  {
-    // Loads of kRoundBatch rounds are issued together, so the rounds wait
-    // for one L2 round trip between them, not one each.
-    constexpr int kRoundBatch = 8;
-    const int items = MP * G * 4;
-    const int rounds = (items + 32 * kMmaWarps - 1) / (32 * kMmaWarps);
-    for (int rd0 = 0; rd0 < rounds; rd0 += kRoundBatch) {
-      uint4 raw[kRoundBatch][2];
+  // Stage the activations, warp by warp: in every chunk of a stage a
+  // consumer warp reads only the B fragments and group sums of its own
+  // GPW groups (gi = c GPC + cw GPW + j), so it stages exactly those and no
+  // warp waits for another.  A quad of lanes (t = 0..3) takes one (batch
+  // row m, group): each lane reads its 16 activations (two 16-byte loads),
+  // forms its 8 B-fragment registers and its part of the group sum; the quad
+  // adds the four parts.  Rows m in [M, MP) are zero.  The first chunk is
+  // staged before any stage is computed; chunk c + 1's loads are issued
+  // before stage (tile 0, c) is computed and converted after it, so their
+  // latency hides behind the math.  Every lane runs the same rounds, so the
+  // quad shuffles always have all 32 lanes.
+  constexpr int kRounds = MP;               // rounds per warp and chunk (GPW <= 8)
+  const int items_w = MP * GPW * 4;
+  const int rounds_w = (items_w + 31) / 32;
+  uint4 raw[kRounds][2];
+  auto stage_load = [&](int c) {
 #pragma unroll
-      for (int i = 0; i < kRoundBatch; ++i) {
-        const int item = (rd0 + i) * 32 * kMmaWarps + cw * 32 + lane;  // item % 4 == t
-        const int mg = item >> 2;
-        const int m = mg / G, gi = mg - m * G;
-        raw[i][0] = raw[i][1] = make_uint4(0u, 0u, 0u, 0u);
-        if (rd0 + i < rounds && item < items && m < M) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K +
-                                                            kbase + gi * 64 + 16 * t);
-          raw[i][0] = src[0];
-          raw[i][1] = src[1];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kRoundBatch; ++i) {
-        if (rd0 + i >= rounds) break;  // uniform across the warp
-        const int item = (rd0 + i) * 32 * kMmaWarps + cw * 32 + lane;
-        const int mg = item >> 2;
-        const int m = mg / G, gi = mg - m * G;
-        const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
-                               raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
-        float part = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-          part += f.x + f.y;
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        uint32_t b[8];
-        bfrag_group<BITS>(w, b);
-        if (item < items) {
-          uint4* dst = xs_frag + (static_cast<size_t>(gi) * 2) * (4 * MP) + m * 4 + t;
-          dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
-          dst[4 * MP] = make_uint4(b[4], b[5], b[6], b[7]);
-          if (t == 0) xs_sum[gi * 8 + m] = part * kTwoM24;
-        }
+    for (int rd = 0; rd < kRounds; ++rd) {
+      raw[rd][0] = raw[rd][1] = make_uint4(0u, 0u, 0u, 0u);
+      const int i = rd * 32 + lane;  // i % 4 == t
+      const int mg = i >> 2;
+      const int m = mg / GPW, gi = c * GPC + cw * GPW + (mg - m * GPW);
+      if (rd < rounds_w && i < items_w && m < M) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * K + kbase + gi * 64 + 16 * t);
+        raw[rd][0] = src[0];
+        raw[rd][1] = src[1];
       }
     }
-    for (int item = cw * 32 + lane; item < (8 - MP) * G; item += 32 * kMmaWarps) {
-      const int m = MP + item / G, gi = item % G;
-      xs_sum[gi * 8 + m] = 0.f;
+  };
+  auto stage_store = [&](int c) {
+#pragma unroll
+    for (int rd = 0; rd < kRounds; ++rd) {
+      if (rd >= rounds_w) break;  // uniform across the warp
+      const int i = rd * 32 + lane;
+      const int mg = i >> 2;
+      const int m = mg / GPW, gi = c * GPC + cw * GPW + (mg - m * GPW);
+      const uint32_t w[8] = {raw[rd][0].x, raw[rd][0].y, raw[rd][0].z, raw[rd][0].w,
+                             raw[rd][1].x, raw[rd][1].y, raw[rd][1].z, raw[rd][1].w};
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        part += f.x + f.y;
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      uint32_t b[8];
+      bfrag_group<BITS>(w, b);
+      if (i < items_w) {
+        uint4* dst = xs_frag + (static_cast<size_t>(gi) * 2) * (4 * MP) + m * 4 + t;
+        dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+        dst[4 * MP] = make_uint4(b[4], b[5], b[6], b[7]);
+        if (t == 0) xs_sum[gi * 8 + m] = part * kTwoM24;
+      }
     }
-  }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&xready_bar));
-  if (!mbar_wait(smem_u32(&xready_bar), 0, &g_status)) return;
+    if constexpr (MP < 8) {
+      constexpr int kPad = 8 - MP;
+      for (int z = lane; z < kPad * GPW; z += 32)  // group sums of the padding rows
+        xs_sum[(c * GPC + cw * GPW + z / kPad) * 8 + MP + z % kPad] = 0.f;
+    }
+    __syncwarp();  // the warp's lanes read each other's fragments
+  };
+  stage_load(0);
+  stage_store(0);
+  if (lane == 0) mbar_arrive(smem_u32(&xready_bar));  // the producer's prefill gate
 
   const bool bl = lane < 4 * MP;  // lanes whose batch row g holds activations
   const int cmask = gm.cswz;
@@ -458,6 +485,8 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   uint32_t phase = 0;
   for (int st = 0; st < nstages; ++st) {
     const int tile = st / NC, c = st - tile * NC;
+    const bool next_x = (tile == 0 && c + 1 < NC);  // stage the next chunk around this one
+    if (next_x) stage_load(c + 1);
     if (!mbar_wait(smem_u32(&full_bar[slot]), phase, &g_status)) return;
     const uint8_t* sb = ring + static_cast<size_t>(slot) * gm.stage_bytes;
 #pragma unroll 2
@@ -466,17 +495,10 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       const int gi = c * GPC + gl;     // group within the row
       uint32_t A0[8], A8[8];           // decoded pairs of rows g and g + 8
       if (BITS == 4) {
-        const uint8_t* p0;
-        const uint8_t* p8;
-        if (DENSE) {
-          p0 = sb + g * gm.ccb + gl * 32 + t * 8;
-          p8 = p0 + 8 * gm.ccb;
-        } else {
-          const uint8_t* box = sb + (gl >> 2) * 2048;
-          const int col = (gl & 3) * 32 + t * 8;
-          p0 = box + swz(g * 128 + col, 0x70);
-          p8 = box + swz((g + 8) * 128 + col, 0x70);
-        }
+        const uint8_t* box = sb + (gl >> 2) * 2048;
+        const int col = (gl & 3) * 32 + t * 8;
+        const uint8_t* p0 = box + swz(g * 128 + col, 0x70);
+        const uint8_t* p8 = box + swz((g + 8) * 128 + col, 0x70);
         const uint2 w0 = *reinterpret_cast<const uint2*>(p0);
         const uint2 w8 = *reinterpret_cast<const uint2*>(p8);
         uint32_t v[4];
@@ -501,17 +523,10 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
         A8[6] = v[1];
         A8[7] = v[3];
       } else {
-        const uint8_t* p0;
-        const uint8_t* p8;
-        if (DENSE) {
-          p0 = sb + g * gm.ccb + gl * 16 + t * 4;
-          p8 = p0 + 8 * gm.ccb;
-        } else {
-          const uint8_t* box = sb + (gl >> 3) * 2048;
-          const int col = (gl & 7) * 16 + t * 4;
-          p0 = box + swz(g * 128 + col, 0x70);
-          p8 = box + swz((g + 8) * 128 + col, 0x70);
-        }
+        const uint8_t* box = sb + (gl >> 3) * 2048;
+        const int col = (gl & 7) * 16 + t * 4;
+        const uint8_t* p0 = box + swz(g * 128 + col, 0x70);
+        const uint8_t* p8 = box + swz((g + 8) * 128 + col, 0x70);
         const uint32_t w0 = *reinterpret_cast<const uint32_t*>(p0);
         const uint32_t w8 = *reinterpret_cast<const uint32_t*>(p8);
         uint32_t v[8];
@@ -539,8 +554,8 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       for (int mi = 0; mi < 4; ++mi)
         mma16816(d, A0[2 * mi], A8[2 * mi], A0[2 * mi + 1], A8[2 * mi + 1], B[2 * mi],
                  B[2 * mi + 1]);
-      const int s0 = DENSE ? g * gm.csb + 2 * gl : swz(g * gm.csb + 2 * gl, cmask);
-      const int s8 = DENSE ? (g + 8) * gm.csb + 2 * gl : swz((g + 8) * gm.csb + 2 * gl, cmask);
+      const int s0 = CHUNKED ? g * gm.csb + 2 * gl : swz(g * gm.csb + 2 * gl, cmask);
+      const int s8 = CHUNKED ? (g + 8) * gm.csb + 2 * gl : swz((g + 8) * gm.csb + 2 * gl, cmask);
       const float sg = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s0));
       const float sg8 = __half2float(*reinterpret_cast<const __half*>(sb + scales_off + s8));
       const float bg = __half2float(*reinterpret_cast<const __half*>(sb + biases_off + s0));
@@ -557,6 +572,7 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
       slot = 0;
       phase ^= 1u;
     }
+    if (next_x) stage_store(c + 1);
     if (c == NC - 1) {  // the tile is complete: hand its partials to the epilogue
       const int b = tile & 1;
       if (!mbar_wait(smem_u32(&redempty_bar[b]), ((tile >> 1) & 1) ^ 1u, &g_status)) return;
@@ -568,35 +584,55 @@ __global__ void __launch_bounds__(64 + 32 * kMmaWarps, 1)
   }
 }
 
-// Stage layout of a shape.  A whole row fits one swizzled stage when its
-// codes are at most 2 KB and its scales 128 bytes (K <= 4096): 16 boxes of
-// 16 rows x 128 B at most, conflict-free fragment loads.  Longer rows are
-// cut into chunks of KC k (the largest multiple of 512 dividing K with
-// codes of at most 2 KB per row), each stage's codes one dense copy of up
-// to 32 KB: the copy engine streams a few large copies per stage much
-// faster than many 2 KB boxes (measured on GB300: one 1-D copy per ring
-// slot reaches ~10 / 19 / 38 / 44 GB/s per SM at 4 / 8 / 16 / 32 KB), which
-// outweighs the 4-way bank conflicts of the unswizzled rows (down
-// 4096 x 14336 at M = 4: 14.8 us dense against 16.7 us in 2 KB boxes; at
-// K = 4096 the boxes win, 6.3 against 7.4 us).
-// (K: the k range of one CTA; with K split across a cluster, dense always:
-// a CTA's part of a row is then too short to fill a stage with boxes.)
-bool dense_layout(int bits, int K, int cl) {
+// Stage layout of a shape.  Rows whose scales fit one 128-byte swizzled box
+// row (K <= 4096, codes at most 2 KB) stream whole: a stage is 16 complete
+// rows, scales and biases as swizzled boxes.  Longer rows (and any row
+// split across a cluster) are cut into chunks of KC k, the longest multiple
+// of 512 up to 4096 that divides the CTA's k range and leaves a ring of two
+// stages; their scales and biases come as plain [16][KC/32] rows.  Either
+// way the codes of a stage are one copy: the copy engine streams a few large
+// copies much faster than many small ones (measured on GB300: one 1-D copy
+// per ring slot reaches ~10 / 19 / 38 / 44 GB/s per SM at 4 / 8 / 16 /
+// 32 KB; down 4096 x 14336 at M = 4: 16.7 us as 2 KB boxes, 14.8 us as one
+// copy per stage).
+// (K: the k range of one CTA.)
+bool chunked_layout(int bits, int K, int cl) {
   return cl > 1 || K * bits / 8 > 2048 || K / 32 > 128;
-}
-
-int choose_kc(int bits, int K, int cl) {
-  if (!dense_layout(bits, K, cl)) return (K % 512 == 0 && K >= 512) ? K : 0;
-  for (int kc = 8 * 2048 / bits; kc >= 512; kc -= 512)
-    if (K % kc == 0) return kc;
-  return 0;
 }
 
 // Bytes of one ring stage for rows of K k cut into chunks of kc.
 int stage_bytes_for(int bits, int K, int kc, int cl) {
   const int ccb = kc * bits / 8, csb = kc / 32;
-  if (dense_layout(bits, K, cl)) return kTileRows * ccb + 2 * ((kTileRows * csb + 127) & ~127);
+  if (chunked_layout(bits, K, cl))  // 1024-byte steps keep every stage's swizzle phase
+    return (kTileRows * ccb + 2 * ((kTileRows * csb + 127) & ~127) + 1023) & ~1023;
   return kTileRows * ccb + 4096;
+}
+
+// Chunk length and ring depth for a CTA's k range of K (whole rows in one
+// stage when they fit a swizzled stage).  Long rows take the longest chunk
+// (a multiple of 512 up to 4096 that divides K) whose ring still holds two
+// stages next to the staged activations: few large copies beat a deeper ring
+// of small ones (measured on GB300, down 4096 x 14336 at M = 4: 32 KB stages
+// two deep 15.3 us, 18 KB stages five deep 17.9 us; M = 8: 9 KB stages ten
+// deep 24.3 against 16.1 us).  false when no chunk fits.
+bool pick_chunk(int bits, int K, int cl, int xs_bytes, int* kc_out, int* stage_out, int* ns_out) {
+  const int budget = dyn_smem_max(cl) - kAlignSlack - xs_bytes - kRedBytes;
+  auto ring = [&](int kc) {
+    const int n = budget / stage_bytes_for(bits, K, kc, cl);
+    return n > kMaxStages ? kMaxStages : n;
+  };
+  int kc = 0;
+  if (!chunked_layout(bits, K, cl)) {
+    if (K % 512 == 0 && K >= 512 && ring(K) >= 2) kc = K;
+  } else {
+    for (int c = 4096; c >= 512 && kc == 0; c -= 512)  // at most 8 groups per warp and stage
+      if (K % c == 0 && ring(c) >= 2) kc = c;
+  }
+  if (kc == 0) return false;
+  *kc_out = kc;
+  *stage_out = stage_bytes_for(bits, K, kc, cl);
+  *ns_out = ring(kc);
+  return true;
 }
 
 // The driver's cuTensorMapEncodeTiled, reached through the runtime.
@@ -620,22 +656,38 @@ EncodeTiledFn encode_fn() {
 
 // 2-D byte-tensor map of `rows` rows of `row_bytes` bytes, boxes of
 // box_bytes x 16 rows with the given swizzle.
-// (elem8: 8-byte elements, so one box row can hold up to 2 KB.)
 bool encode_rows(CUtensorMap* m, const void* base, long long rows, int row_bytes, int box_bytes,
-                 CUtensorMapSwizzle swizzle, bool elem8 = false) {
+                 CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const int es = elem8 ? 8 : 1;
-  const cuuint64_t dim[2] = {static_cast<cuuint64_t>(row_bytes / es),
-                             static_cast<cuuint64_t>(rows)};
+  const cuuint64_t dim[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   const cuuint64_t stride[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / es),
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes),
                              static_cast<cuuint32_t>(kTileRows)};
   const cuuint32_t estride[2] = {1, 1};
-  return fn(m, elem8 ? CU_TENSOR_MAP_DATA_TYPE_UINT64 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-            const_cast<void*>(base), dim, stride, box,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dim, stride, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D byte-tensor map of a code matrix seen as 128-byte columns: x the byte
+// within a column (128), y the row (stride row_bytes), z the column (stride
+// 128 B).  A box of {128, 16, ccb / 128} lands in shared memory as
+// [column][row][128 B] with the 128-byte swizzle: the layout of 16-row x
+// 128 B boxes laid side by side, delivered by one copy.
+bool encode_code_columns(CUtensorMap* m, const void* base, long long rows, int row_bytes,
+                         int ccb) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || row_bytes % 128 != 0 || ccb % 128 != 0 || ccb / 128 > 256) return false;
+  const cuuint64_t dim[3] = {128, static_cast<cuuint64_t>(rows),
+                             static_cast<cuuint64_t>(row_bytes / 128)};
+  const cuuint64_t stride[2] = {static_cast<cuuint64_t>(row_bytes), 128};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kTileRows),
+                             static_cast<cuuint32_t>(ccb / 128)};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dim, stride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Clusters of `cl` CTAs of this kernel that can be resident at once, for a
@@ -650,7 +702,7 @@ int resident_clusters(F* k, int cl, int smem, int device) {
     if (dev_of[i] == device && smem_of[i] == smem) return val_of[i];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cl));
-  cfg.blockDim = dim3(64 + 32 * kMmaWarps);
+  cfg.blockDim = dim3(kBlockThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -671,12 +723,12 @@ int resident_clusters(F* k, int cl, int smem, int device) {
   return n;
 }
 
-template <int BITS, int MP, bool DENSE, int CL>
+template <int BITS, int MP, bool CHUNKED, int CL>
 cudaError_t launch_mma_t(const StreamArgs& a, MmaGeom gm, const CUtensorMap* maps,
                          cudaStream_t stream, int device) {
   static unsigned done_mask = 0;
-  auto* k = batch_mma_kernel<BITS, MP, DENSE, CL>;
-  cudaError_t e = ensure_smem_attr(k, kDynSmemMax, &done_mask, device);
+  auto* k = batch_mma_kernel<BITS, MP, CHUNKED, CL>;
+  cudaError_t e = ensure_smem_attr(k, dyn_smem_max(CL), &done_mask, device);
   if (e != cudaSuccess) return e;
   int clusters = gm.grid;  // one CTA per SM and cluster rank
   if (CL > 1) {
@@ -687,7 +739,7 @@ cudaError_t launch_mma_t(const StreamArgs& a, MmaGeom gm, const CUtensorMap* map
   gm.grid = clusters * CL;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gm.grid));
-  cfg.blockDim = dim3(64 + 32 * kMmaWarps);
+  cfg.blockDim = dim3(kBlockThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(gm.smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -721,13 +773,8 @@ bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, i
   if (Kc % (64 * kMmaWarps) != 0 || Kc < 64 * kMmaWarps) return false;
   const int xs_bytes = xs_of(cl);
   if (xs_bytes > kXsBudget) return false;
-  const int kc = choose_kc(bits, Kc, cl);
-  if (kc == 0) return false;
-  const int stage = stage_bytes_for(bits, Kc, kc, cl);
-  const int budget = kDynSmemMax - kAlignSlack - xs_bytes - kRedBytes;
-  int ns = budget / stage;
-  if (ns > kMaxStages) ns = kMaxStages;
-  if (ns < 2) return false;
+  int kc = 0, stage = 0, ns = 0;
+  if (!pick_chunk(bits, Kc, cl, xs_bytes, &kc, &stage, &ns)) return false;
   *mp_out = mp;
   *smem_out = kAlignSlack + ns * stage + xs_bytes + kRedBytes;
   *ns_out = ns;
@@ -743,21 +790,24 @@ cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_
   MmaGeom gm{};
   gm.cl = cl;
   const int Kc = a.K / cl;
-  gm.kc = choose_kc(bits, Kc, cl);
+  const int xs_bytes = 2 * mp * Kc + Kc / 2;
+  int stage = 0, ns2 = 0;
+  if (!pick_chunk(bits, Kc, cl, xs_bytes, &gm.kc, &stage, &ns2) || ns2 != ns)
+    return cudaErrorNotSupported;
   gm.ccb = gm.kc * bits / 8;
   gm.csb = gm.kc / 32;
   // scale / bias boxes: a swizzle span equal to the row when the row is 32,
   // 64 or 128 bytes, else none
   gm.cswz = gm.csb == 128 ? 0x70 : (gm.csb == 64 ? 0x30 : (gm.csb == 32 ? 0x10 : 0));
-  gm.stage_bytes = stage_bytes_for(bits, Kc, gm.kc, cl);
+  gm.stage_bytes = stage;
   gm.ns = ns;
   gm.smem_bytes = smem;
   const long long tiles = (a.rows + kTileRows - 1) / kTileRows;
   gm.tiles = static_cast<int>(tiles);
   gm.grid = static_cast<int>(tiles < sms ? tiles : sms);
   gm.prefill = prefill_stages(gm.stage_bytes, ns);
-  const bool dense = dense_layout(bits, Kc, cl);
-  if (dense) gm.cswz = 0;
+  const bool chunked = chunked_layout(bits, Kc, cl);
+  if (chunked) gm.cswz = 0;
   const CUtensorMapSwizzle ssw = gm.cswz == 0x70   ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : gm.cswz == 0x30 ? CU_TENSOR_MAP_SWIZZLE_64B
                                  : gm.cswz == 0x10 ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -765,14 +815,12 @@ cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_
   CUtensorMap maps[3];
   const int rcb = a.K * bits / 8, rgb = a.K / 32;
   const bool ok_maps =
-      (dense ? encode_rows(&maps[0], a.codes[0], a.rows, rcb, gm.ccb, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           true)
-             : encode_rows(&maps[0], a.codes[0], a.rows, rcb, 128, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+      encode_code_columns(&maps[0], a.codes[0], a.rows, rcb, gm.ccb) &&
       encode_rows(&maps[1], a.scales[0], a.rows, rgb, gm.csb, ssw) &&
       encode_rows(&maps[2], a.biases[0], a.rows, rgb, gm.csb, ssw);
   if (!ok_maps) return cudaErrorInvalidValue;
 #define QGEMV_MMA_LAUNCH(B, P)                                                  \
-  return !dense     ? launch_mma_t<B, P, false, 1>(a, gm, maps, st, device)  \
+  return !chunked   ? launch_mma_t<B, P, false, 1>(a, gm, maps, st, device)  \
          : cl == 1  ? launch_mma_t<B, P, true, 1>(a, gm, maps, st, device)   \
          : cl == 2  ? launch_mma_t<B, P, true, 2>(a, gm, maps, st, device)   \
                     : launch_mma_t<B, P, true, 4>(a, gm, maps, st, device)
