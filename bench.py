@@ -665,9 +665,9 @@ def run_one_op(args, name):
         def call(w):
             for wi, xi_, yi in zip(w, xs, ys):
                 fn(wi, xi_, y=yi)
-        # at M = 8 the down projection's activations (2 * 8 * 14336 bytes) do
-        # not fit the tensor-core kernel's shared memory: two 4-row passes
-        launches = 3 if M == 8 else 2
+        # one launch per matrix (at M = 8 the down projection splits K over
+        # clusters of two CTAs inside its one launch)
+        launches = 2
     elif name == "residual_rmsnorm":
         config = "residual add + RMSNorm epilogue, hidden 4096 (qgemv_residual_rmsnorm)"
         K = H
