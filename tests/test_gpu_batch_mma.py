@@ -1,16 +1,17 @@
 """The small-batch GEMV (M = 2..8) against the oracle.
 
 M >= 3 runs on the tensor-core kernel, which stages the batch's activations
-in shared memory (2 * M_pad * K bytes, M_pad = 4 or 8): one pass when they
-fit, else passes of at most 4 rows (a last pass of two rows takes the
-CUDA-core small-batch kernel, of one row the M = 1 streaming kernel); M = 2
-runs on the CUDA-core small-batch kernel.  Shapes here
-cover every plan: stages of 512 to 4096 k, ragged 16-row tiles, bands of a
-few rows, K = 8192 at M = 8 in one pass, K = 14336 at M = 5..8 in two passes,
-residuals, 2-bit codes, exact integer dots (scale 1, bias 0, x in {-1, 0,
-1}), and activations whose pre-divided copies (x / 16, x / 64) are fp16
-subnormals.  Every output is checked against the fp64 oracle within the
-matvec tolerance, and each batch row against the M = 1 call on that row.
+in shared memory (2 * M_pad * K bytes, M_pad = 4 or 8): one CTA per tile
+when they fit, else K split over a thread-block cluster of 2 or 4 CTAs whose
+fp32 partials meet in rank 0 (M >= 5 at K = 14336, every M >= 3 at K =
+16384 and 32768), and passes of at most 4 rows only when even that cannot hold them;
+M = 2 runs on the CUDA-core small-batch kernel.  Shapes here cover every
+plan: whole rows of 512 to 4096 k in one stage, chunked rows, ragged 16-row
+tiles, bands of a few rows, cluster splits of 2 and 4, residuals, 2-bit
+codes, exact integer dots (scale 1, bias 0, x in {-1, 0, 1}), and
+activations whose pre-divided copies (x / 16, x / 64) are fp16 subnormals.
+Every output is checked against the fp64 oracle within the matvec
+tolerance, and each batch row against the M = 1 call on that row.
 """
 import numpy as np
 import pytest
@@ -105,4 +106,24 @@ def test_batch_inplace_residual_and_guards():
     assert np.all(raw[:G] == 0x7E5A) and np.all(raw[G + M * N:] == 0x7E5A)
     y64, _, bound = oracle.qgemv(4, w.codes, w.scales, w.biases, x, r)
     check(yv, y64, plain_tol(bound), "in-place residual")
+    assert q.device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 1003, 14336), (5, 77, 32768)])
+def test_batch_cluster_split_inplace_residual_and_guards(M, N, K):
+    """The cluster-split path (rank 0 adds the other ranks' partials and
+    writes y) with y aliasing the residual, inside guard bands."""
+    w = W(13 + K, N, K, 4)
+    x = X(14 + K, K, M)
+    r = X(15 + N, N, M)
+    G = 256
+    buf = torch.full((M * N + 2 * G,), 0x7E5A, dtype=torch.int16, device="cuda")
+    yv = buf[G:G + M * N].view(torch.float16).view(M, N)
+    yv.copy_(dev16(r))
+    q.qgemv_w4g64(dev_weight(w), dev16(x), y=yv, residual=yv)
+    torch.cuda.synchronize()
+    raw = buf.cpu().numpy()
+    assert np.all(raw[:G] == 0x7E5A) and np.all(raw[G + M * N:] == 0x7E5A)
+    y64, _, bound = oracle.qgemv(4, w.codes, w.scales, w.biases, x, r)
+    check(yv, y64, plain_tol(bound), f"cluster split M={M} K={K}")
     assert q.device_status() == 0
