@@ -43,20 +43,27 @@ namespace {
 constexpr int kMmaWarps = 8;                 // consumer warps
 constexpr int kTileRows = 16;                // rows of one MMA tile (and one stage)
 constexpr int kXsBudget = 132 * 1024;        // activation fragments + group sums
-// K is split over a cluster only when one CTA cannot hold the activations:
-// measured on GB300 (graph replays), splitting when they fit anyway was
-// slower (M = 8, 4096 x 4096: 7.9 us split in 2 against 6.3 us whole; M = 4,
-// 4096 x 14336: 15.4 against 14.9 us), while M = 8 at K = 14336, which does
-// not fit, went from two passes (29.0 us) to one split pass (16.9 us).
+// K is split over a cluster of 4 when one CTA would stage more than 96 KB
+// of activations (every CTA takes in all of them beside its weights: a
+// quarter each is cheaper than the exchange of partials), else kept whole
+// unless it does not fit.  Measured on GB300 (graph replays, 4096 rows,
+// 4-bit; whole / split in 2 / split in 4): K = 8192, M = 4 10.8 / 10.7 /
+// 11.8 us (68 KB: kept whole), M = 8 13.8 / 12.2 / 11.8; K = 14336, M = 4
+// 14.9 / 14.2 / 13.8, M = 8 (does not fit whole) 16.0 / 15.1; K = 16384,
+// M = 8 21.5 / 19.7; K = 4096, M = 8 6.3 whole against 7.9 split in 2.
+constexpr int kSplitAbove = 96 * 1024;
 constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;  // two tiles of warp partials
 constexpr int kSmemPerBlock = 227 * 1024;    // sm_100-family opt-in shared memory per block
 // Dynamic shared memory of a CTA in a cluster of cl: what the block may
 // hold less a bound on the kernel's static part (barriers, 384 bytes, and
-// for cl > 1 the cluster exchange slots, 1 KB per rank).  Every byte counts:
+// for cl > 1 the cluster exchange slots, 512 bytes per slot and rank).  Every byte counts:
 // for M = 4 at K = 14336 the staged activations take 119 KB, and what is
 // left holds a third 32 KB stage only at the full limit (measured on GB300,
 // down 4096 x 14336: two stages 15.3 us).
-constexpr int dyn_smem_max(int cl) { return kSmemPerBlock - 512 - (cl > 1 ? 1024 * cl : 0); }
+constexpr int kXSlots = 4;  // cluster exchange slots: ranks run up to 4 tiles ahead of rank 0
+constexpr int dyn_smem_max(int cl) {
+  return kSmemPerBlock - 512 - (cl > 1 ? kXSlots * 512 * cl : 0);
+}
 // Threads of a CTA: producer warp, epilogue warp, the consumer warps.
 constexpr int kBlockThreads = 64 + 32 * kMmaWarps;
 constexpr int kAlignSlack = 1024;            // the ring starts on a 1024-byte boundary
@@ -146,10 +153,14 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t r) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(r));
   return out;
 }
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
+// 16 bytes into another CTA's shared memory, completing 16 bytes of the
+// transaction count of that CTA's mbarrier (no fence, no arrive).
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+      : "memory");
 }
 __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
@@ -239,10 +250,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
   __shared__ __align__(8) uint64_t redempty_bar[2];
   __shared__ __align__(8) uint64_t xready_bar;
   // cluster split of K (CL > 1): rank 0 collects the other ranks' tile
-  // partials (cfull) and hands the slots back (cempty, on the other ranks)
-  __shared__ __align__(8) uint64_t cfull_bar[2];
-  __shared__ __align__(8) uint64_t cempty_bar[2];
-  __shared__ __align__(16) float4 xred[CL > 1 ? 2 * CL * 32 : 1];
+  // partials (cfull: rank 0's own arrive with the expected bytes, the other
+  // ranks' asynchronous stores completing them) and hands the slots back
+  // (cempty, on the other ranks)
+  __shared__ __align__(8) uint64_t cfull_bar[kXSlots];
+  __shared__ __align__(8) uint64_t cempty_bar[kXSlots];
+  __shared__ __align__(16) float4 xred[CL > 1 ? kXSlots * CL * 32 : 1];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -295,8 +308,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
       mbar_init(smem_u32(&redempty_bar[b]), 1);
     }
     mbar_init(smem_u32(&xready_bar), kMmaWarps);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&cfull_bar[b]), 32 * (CL - 1 > 0 ? CL - 1 : 1));
+    for (int b = 0; b < kXSlots; ++b) {
+      mbar_init(smem_u32(&cfull_bar[b]), 1);
       mbar_init(smem_u32(&cempty_bar[b]), 1);
     }
     fence_mbar_init();
@@ -379,29 +392,33 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&redempty_bar[b]));
       if (CL > 1) {
+        const int x = tile % kXSlots;                         // exchange slot
+        const uint32_t xph = static_cast<uint32_t>(tile / kXSlots) & 1u;  // its phase
         if (rank != 0) {
-          // hand this CTA's partial of the tile to rank 0 (its slot b, once
-          // rank 0 has read the tile two back from it)
-          if (tile >= 2 &&
-              !mbar_wait_cluster(smem_u32(&cempty_bar[b]), ((tile >> 1) & 1) ^ 1u, &g_status))
+          // hand this CTA's partial of the tile to rank 0 (slot x, once rank
+          // 0 has read the tile kXSlots back from it)
+          if (tile >= kXSlots &&
+              !mbar_wait_cluster(smem_u32(&cempty_bar[x]), xph ^ 1u, &g_status))
             return;
-          const uint32_t dst = map_to_rank(smem_u32(&xred[(b * CL + rank) * 32 + lane]), 0);
-          st_cluster_f4(dst, make_float4(v[0], v[1], v[2], v[3]));
-          arrive_remote(map_to_rank(smem_u32(&cfull_bar[b]), 0));
+          st_async_f4(map_to_rank(smem_u32(&xred[(x * CL + rank) * 32 + lane]), 0),
+                      make_float4(v[0], v[1], v[2], v[3]), map_to_rank(smem_u32(&cfull_bar[x]), 0));
           continue;
         }
-        // rank 0: add the other ranks' partials, in rank order
-        if (!mbar_wait_cluster(smem_u32(&cfull_bar[b]), (tile >> 1) & 1, &g_status)) return;
+        // rank 0: add the other ranks' partials, in rank order, once their
+        // (CL - 1) x 512 bytes have landed (the transaction count may run
+        // ahead of this expectation; the phase needs both)
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&cfull_bar[x]), (CL - 1) * 32 * 16);
+        if (!mbar_wait_cluster(smem_u32(&cfull_bar[x]), xph, &g_status)) return;
         for (int r = 1; r < CL; ++r) {
-          const float4 p = xred[(b * CL + r) * 32 + lane];
+          const float4 p = xred[(x * CL + r) * 32 + lane];
           v[0] += p.x;
           v[1] += p.y;
           v[2] += p.z;
           v[3] += p.w;
         }
         __syncwarp();
-        if (lane == 0 && tile + 2 < ntiles)  // the slot is reused: hand it back
-          for (int r = 1; r < CL; ++r) arrive_remote(map_to_rank(smem_u32(&cempty_bar[b]), r));
+        if (lane == 0 && tile + kXSlots < ntiles)  // the slot is reused: hand it back
+          for (int r = 1; r < CL; ++r) arrive_remote(map_to_rank(smem_u32(&cempty_bar[x]), r));
       }
       store_tile(tile, v);
     }
@@ -768,11 +785,13 @@ bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, i
                     int* ns_out, int* cl_out) {
   if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
   const int mp = M <= 4 ? 4 : 8;
-  // Split K across a cluster (2, then 4 CTAs) while one CTA cannot hold
-  // the staged activations.
+  // Split K across a cluster: into 4 when the activations of a whole row
+  // are large (kSplitAbove), else only while one CTA cannot hold them.
   auto xs_of = [&](int c) { return 2 * mp * (K / c) + (K / c) / 2; };  // fragments + group sums
+  auto splits = [&](int c) { return K % (c * 64 * kMmaWarps) == 0; };
   int cl = 1;
-  while (cl < 4 && xs_of(cl) > kXsBudget && K % (2 * cl * 64 * kMmaWarps) == 0) cl *= 2;
+  if (xs_of(1) > kSplitAbove) cl = splits(4) ? 4 : (splits(2) ? 2 : 1);
+  while (cl < 4 && xs_of(cl) > kXsBudget && splits(2 * cl)) cl *= 2;
   const int Kc = K / cl;
   if (Kc % (64 * kMmaWarps) != 0 || Kc < 64 * kMmaWarps) return false;
   const int xs_bytes = xs_of(cl);
