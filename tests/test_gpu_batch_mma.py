@@ -47,6 +47,7 @@ def run(bits, w, x, r=None):
     (8, 4096, 14336), (6, 2, 2048), (8, 1, 1024), (2, 151936 // 8, 1024),
     (4, 300, 16384), (8, 333, 16384), (5, 97, 32768), (3, 40, 32768),
     (8, 1, 14336), (4, 1, 14336), (5, 4096 + 15, 8192),
+    (8, 151936 // 4, 1024), (4, 1024, 3072), (6, 3072, 1024),
 ])
 def test_batch_parity(bits, M, N, K):
     w = W(N + K + M + bits, N, K, bits)
