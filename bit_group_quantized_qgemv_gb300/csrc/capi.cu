@@ -110,9 +110,10 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
     if (p.ok && al16) return finish(qgemv::stream_plain(bits, p, a, st, dev));
     return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
   }
-  // Small batch on the tensor cores (M >= 3): one pass holding all M rows
-  // when their activations fit in shared memory, else passes of at most 4
-  // rows (a pass of 1 or 2 rows takes the CUDA-core kernels).
+  // Small batch on the tensor cores (M >= 3, and M = 2 on short ops): one
+  // pass holding all M rows when their activations fit in shared memory,
+  // else passes of at most 4 rows (a pass of 1 or 2 rows takes the
+  // CUDA-core kernels).
   int mp = 0, smem = 0, ns = 0, cl = 1;
   if (al16 && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl))
     return finish(qgemv::stream_batch_mma(bits, a, sms, st, dev));

@@ -67,12 +67,18 @@ constexpr int dyn_smem_max(int cl) {
 // Threads of a CTA: producer warp, epilogue warp, the consumer warps.
 constexpr int kBlockThreads = 64 + 32 * kMmaWarps;
 constexpr int kAlignSlack = 1024;            // the ring starts on a 1024-byte boundary
-// Smallest batch the tensor-core kernel takes.  Measured on GB300 (graph
-// replays, o_proj 4096x4096 + down 4096x14336, 4-bit): M = 2 took 21.1 us
-// here against 17.4 us for the CUDA-core kernel, whose 2 FMAs per weight
-// are cheap; from M = 3 up the tensor cores are faster (M = 4: 22.9 against
-// 25.6 us; M = 8: 40.0 against 45.8 us).
-constexpr int kMmaMinM = 3;
+// From M = 3 up the tensor cores are faster than the CUDA-core small-batch
+// kernel on every shape (graph replays on GB300, o_proj 4096x4096 + down
+// 4096x14336, 4-bit: M = 4 19.8 against 25.6 us; M = 8 21.9 against 45.8).
+// At M = 2 the CUDA-core kernel's 2 FMAs per weight are cheap and it
+// streams long ops better, while the tensor-core kernel's shorter start
+// wins on short ones: M = 2 takes the tensor cores only for K <= 4096 and
+// at most kMma2Bytes of weights per SM (4096x4096 5.21 against 5.72 us,
+// 6144x4096 6.61 / 7.10, 1024x1024 2.29 / 3.98, 3072x1024 3.55 / 4.18; but
+// 14336x4096 11.14 / 10.88, 4096x8192 10.61 / 8.29, 4096x14336 13.62 /
+// 11.65).
+constexpr int kMmaMinM = 2;
+constexpr long long kMma2Bytes = 128 * 1024;
 
 // Geometry of one launch (host-side plan, passed to the kernel).
 struct MmaGeom {
@@ -784,6 +790,8 @@ cudaError_t launch_mma_t(const StreamArgs& a, MmaGeom gm, const CUtensorMap* map
 bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, int* smem_out,
                     int* ns_out, int* cl_out) {
   if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
+  if (M == 2 && (K > 4096 || N * (static_cast<long long>(K) * bits / 8 + K / 32) > kMma2Bytes * sms))
+    return false;
   const int mp = M <= 4 ? 4 : 8;
   // Split K across a cluster: into 4 when the activations of a whole row
   // are large (kSplitAbove), else only while one CTA cannot hold them.

@@ -1,17 +1,19 @@
 """The small-batch GEMV (M = 2..8) against the oracle.
 
-M >= 3 runs on the tensor-core kernel, which stages the batch's activations
+M >= 3 runs on the tensor-core kernel, and so does M = 2 on short ops (K <=
+4096, at most 128 KB of weights per SM; longer ones take the CUDA-core
+small-batch kernel).  The tensor-core kernel stages the batch's activations
 in shared memory (2 * M_pad * K bytes, M_pad = 4 or 8): one CTA per tile
-when they fit, else K split over a thread-block cluster of 2 or 4 CTAs whose
-fp32 partials meet in rank 0 (M >= 5 at K = 14336, every M >= 3 at K =
-16384 and 32768), and passes of at most 4 rows only when even that cannot hold them;
-M = 2 runs on the CUDA-core small-batch kernel.  Shapes here cover every
-plan: whole rows of 512 to 4096 k in one stage, chunked rows, ragged 16-row
-tiles, bands of a few rows, cluster splits of 2 and 4, residuals, 2-bit
-codes, exact integer dots (scale 1, bias 0, x in {-1, 0, 1}), and
-activations whose pre-divided copies (x / 16, x / 64) are fp16 subnormals.
-Every output is checked against the fp64 oracle within the matvec
-tolerance, and each batch row against the M = 1 call on that row.
+when they are small, else K split over a thread-block cluster of 4 (or 2)
+CTAs whose fp32 partials meet in rank 0 (M >= 5 from K = 8192, every M >=
+3 from K = 14336), and passes of at most 4 rows only when even that cannot
+hold them.  Shapes here cover every plan: whole rows of 512 to 4096 k in
+one stage, chunked rows, ragged 16-row tiles, bands of a few rows, cluster
+splits, residuals, 2-bit codes, exact integer dots (scale 1, bias 0, x in
+{-1, 0, 1}), and activations whose pre-divided copies (x / 16, x / 64) are
+fp16 subnormals.  Every output is checked against the fp64 oracle within
+the matvec tolerance, and each batch row against the M = 1 call on that
+row.
 """
 import numpy as np
 import pytest
