@@ -114,10 +114,18 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
   // pass holding all M rows when their activations fit in shared memory,
   // else passes of at most 4 rows (a pass of 1 or 2 rows takes the
   // CUDA-core kernels).
+  // (cudaErrorNotSupported: the device cannot host the plan's clusters, say
+  // under a restricted SM partition; nothing was launched, so the CUDA-core
+  // kernels below take the call.)
   int mp = 0, smem = 0, ns = 0, cl = 1;
-  if (al16 && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl))
-    return finish(qgemv::stream_batch_mma(bits, a, sms, st, dev));
-  if (al16 && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns, &cl)) {
+  bool mma_ok = al16;
+  if (mma_ok && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl)) {
+    const cudaError_t e = qgemv::stream_batch_mma(bits, a, sms, st, dev);
+    if (e != cudaErrorNotSupported) return finish(e);
+    cudaGetLastError();
+    mma_ok = false;
+  }
+  if (mma_ok && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns, &cl)) {
     for (int m0 = 0; m0 < M; m0 += 4) {
       StreamArgs ap = a;
       ap.M = M - m0 < 4 ? M - m0 : 4;
