@@ -56,10 +56,8 @@ constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;  // two tiles of warp partial
 constexpr int kSmemPerBlock = 227 * 1024;    // sm_100-family opt-in shared memory per block
 // Dynamic shared memory of a CTA in a cluster of cl: what the block may
 // hold less a bound on the kernel's static part (barriers, 384 bytes, and
-// for cl > 1 the cluster exchange slots, 512 bytes per slot and rank).  Every byte counts:
-// for M = 4 at K = 14336 the staged activations take 119 KB, and what is
-// left holds a third 32 KB stage only at the full limit (measured on GB300,
-// down 4096 x 14336: two stages 15.3 us).
+// for cl > 1 the cluster exchange slots, 512 bytes per slot and rank); the
+// ring takes all that the staged activations leave.
 constexpr int kXSlots = 4;  // cluster exchange slots: ranks run up to 4 tiles ahead of rank 0
 constexpr int dyn_smem_max(int cl) {
   return kSmemPerBlock - 512 - (cl > 1 ? kXSlots * 512 * cl : 0);
