@@ -131,3 +131,19 @@ def test_batch_cluster_split_inplace_residual_and_guards(M, N, K):
     y64, _, bound = oracle.qgemv(4, w.codes, w.scales, w.biases, x, r)
     check(yv, y64, plain_tol(bound), f"cluster split M={M} K={K}")
     assert q.device_status() == 0
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_batch_misaligned_activations_take_generic_path(M):
+    """Activations 2 bytes off a 16-byte boundary: neither small-batch
+    kernel applies (both read x with 16-byte loads), the generic kernel
+    takes the call, same results."""
+    N, K = 301, 4096
+    w = W(21 + M, N, K, 4)
+    x = X(22 + M, K, M)
+    flat = np.concatenate([[0], x.reshape(-1)]).astype(np.float16)
+    xd = dev16(flat)[1:].view(M, K)
+    assert xd.data_ptr() % 16 == 2
+    y = q.qgemv_w4g64(dev_weight(w), xd)
+    y64, _, bound = oracle.qgemv(4, w.codes, w.scales, w.biases, x)
+    check(y, y64, plain_tol(bound), f"misaligned M={M}")
