@@ -62,7 +62,8 @@ def parse_args():
                    help="time one op or configuration unit alone instead of the stack: "
                         "qkv, o_proj, swiglu, down, moe, moe_routed, lm_head, lm_head_argmax, "
                         "lm_head_sample, gemv1024, lut_layer, lut_lm_head, "
-                        "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m8_w2, residual_rmsnorm, "
+                        "qwen_stack, w2_layer, w8_layer, m2, m4, m8, m2_w2, m4_w2, m8_w2, "
+                        "residual_rmsnorm, "
                         "or all")
     p.add_argument("--copies", type=int, default=0,
                    help="--op: device copies of the weights to rotate through (default: "
@@ -488,7 +489,8 @@ def run_own(args):
 
 OPS = ["qkv", "o_proj", "swiglu", "down", "moe", "moe_routed", "lm_head", "lm_head_argmax",
        "lm_head_sample", "gemv1024", "lut_layer", "lut_lm_head",
-       "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m8_w2", "residual_rmsnorm"]
+       "qwen_stack", "w2_layer", "w8_layer", "m2", "m4", "m8", "m2_w2", "m4_w2", "m8_w2",
+       "residual_rmsnorm"]
 
 
 def run_op(args):
@@ -650,7 +652,7 @@ def run_one_op(args, name):
             for (key, n, k), wi, rows in zip(shapes, w, rpl):
                 q.qgemv_lut4(wi[0], wi[1], xs[k], rows_per_lut=rows, y=y[:n])
         launches = len(shapes)
-    elif name in ("m2", "m4", "m8", "m8_w2"):
+    elif name in ("m2", "m4", "m8", "m2_w2", "m4_w2", "m8_w2"):
         M = int(name[1])
         bits = 2 if name.endswith("w2") else 4
         config = "config 4: M=%d small batch, %d-bit, o_proj- and down-shaped" % (M, bits)
