@@ -715,16 +715,24 @@ bool encode_code_columns(CUtensorMap* m, const void* base, long long rows, int r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters of `cl` CTAs of this kernel that can be resident at once, for a
-// shared-memory size (cudaOccupancyMaxActiveClusters, cached per device).
+// Clusters of `cl` CTAs of kernel k that can be resident at once with smem
+// bytes of dynamic shared memory (cudaOccupancyMaxActiveClusters), cached per
+// (kernel, cluster size, shared memory, device); a failed query is not
+// cached and reads as 0.
 template <typename F>
 int resident_clusters(F* k, int cl, int smem, int device) {
+  struct Entry {
+    const void* k;
+    int cl, smem, device, n;
+  };
   static std::mutex mu;
-  static int dev_of[8] = {-1, -1, -1, -1, -1, -1, -1, -1}, smem_of[8], val_of[8];
+  static Entry cache[16] = {};
   static int next = 0;
   std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < 8; ++i)
-    if (dev_of[i] == device && smem_of[i] == smem) return val_of[i];
+  for (const Entry& e : cache)
+    if (e.k == reinterpret_cast<const void*>(k) && e.cl == cl && e.smem == smem &&
+        e.device == device)
+      return e.n;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cl));
   cfg.blockDim = dim3(kBlockThreads);
@@ -737,14 +745,12 @@ int resident_clusters(F* k, int cl, int smem, int device) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
-    n = 0;
+    return 0;
   }
-  dev_of[next] = device;
-  smem_of[next] = smem;
-  val_of[next] = n;
-  next = (next + 1) % 8;
+  cache[next] = Entry{reinterpret_cast<const void*>(k), cl, smem, device, n};
+  next = (next + 1) % 16;
   return n;
 }
 
