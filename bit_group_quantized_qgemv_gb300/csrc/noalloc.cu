@@ -43,25 +43,33 @@ using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
 // The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime (the
-// library does not link the driver library itself).
+// library does not link the driver library itself); looked up once,
+// thread-safely.
 bool driver_ctx_fns(CtxGetCurrentFn* cur, CtxGetIdFn* id) {
-  static CtxGetCurrentFn s_cur = nullptr;
-  static CtxGetIdFn s_id = nullptr;
-  if (s_cur == nullptr || s_id == nullptr) {
+  struct Fns {
+    CtxGetCurrentFn cur = nullptr;
+    CtxGetIdFn id = nullptr;
+  };
+  static const Fns fns = [] {
+    Fns r;
     void* f0 = nullptr;
     void* f1 = nullptr;
     cudaDriverEntryPointQueryResult q0, q1;
     if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault,
-                                         &q0) != cudaSuccess ||
-        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) !=
-            cudaSuccess ||
-        q0 != cudaDriverEntryPointSuccess || q1 != cudaDriverEntryPointSuccess || !f0 || !f1)
-      return false;
-    s_cur = reinterpret_cast<CtxGetCurrentFn>(f0);
-    s_id = reinterpret_cast<CtxGetIdFn>(f1);
-  }
-  *cur = s_cur;
-  *id = s_id;
+                                         &q0) == cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q0 == cudaDriverEntryPointSuccess && q1 == cudaDriverEntryPointSuccess && f0 && f1) {
+      r.cur = reinterpret_cast<CtxGetCurrentFn>(f0);
+      r.id = reinterpret_cast<CtxGetIdFn>(f1);
+    } else {
+      cudaGetLastError();
+    }
+    return r;
+  }();
+  if (fns.cur == nullptr || fns.id == nullptr) return false;
+  *cur = fns.cur;
+  *id = fns.id;
   return true;
 }
 

@@ -666,16 +666,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// (looked up once, thread-safely; null when the driver does not provide it)
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static const EncodeTiledFn fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult qr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                          &qr) == cudaSuccess &&
         qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
+      return reinterpret_cast<EncodeTiledFn>(f);
+    cudaGetLastError();
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
