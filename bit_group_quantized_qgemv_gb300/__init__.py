@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     lm_head_argmax,
     lm_head_sample,
     argmax_scratch_bytes,
+    plan_gemv,
     moe_qgemv_combine,
     moe_qgemv_combine_traced,
     moe_router,

@@ -48,7 +48,18 @@ _SIGS = {
     "qgemv_sample_topk": (_I, [_P, _I, _I, _F, _P, _P, _P, _P, _P]),
     "qgemv_lut4": (_I, [_P, _P, _I, _I, _P, _P, _I, _I, _P, _P]),
     "qgemv_lm_head_sample": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "qgemv_plan_gemv": (_I, [_I, _I, _I, _I, _I, _I, _P]),
 }
+
+
+class GemvPlan(ctypes.Structure):
+    """qgemv_gemv_plan (include/qgemv.h)."""
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("path", "passes", "m_pad", "cluster", "chunk_k", "stages", "smem_bytes")]
+
+
+#: QGEMV_PATH_* of include/qgemv.h, by value.
+GEMV_PATHS = ("generic", "stream", "mma", "mma_passes", "batch", "batch_passes")
 
 #: Names the C header declares (the binding exposes each one).
 EXPORTED = tuple(_SIGS)
@@ -186,6 +197,17 @@ def moe_router(w, x, top_k=4, shared=0, logits=None, idx=None, wt=None, stream=N
 
 def argmax_scratch_bytes() -> int:
     return int(lib.qgemv_argmax_scratch_bytes())
+
+
+def plan_gemv(bits, M, N, K, sms, aligned16=True):
+    """The kernels qgemv_w4g64 / w2g64 / w8g64 take for a shape
+    (qgemv_plan_gemv; host-only): a dict with the path name and its plan."""
+    out = GemvPlan()
+    _check(lib.qgemv_plan_gemv(int(bits), int(M), int(N), int(K), int(sms), int(bool(aligned16)),
+                               ctypes.byref(out)), "qgemv_plan_gemv")
+    d = {n: getattr(out, n) for n, _ in GemvPlan._fields_}
+    d["path"] = GEMV_PATHS[d["path"]]
+    return d
 
 
 def lm_head_argmax(w, x, logits=None, scratch=None, token=None, stream=None):

@@ -82,6 +82,59 @@ StreamArgs blank_args() {
   return a;
 }
 
+// Which kernels a qgemv_w4g64 / w2g64 / w8g64 call of this shape takes
+// (plain_impl follows it; qgemv_plan_gemv reports it).  al16: codes, scales,
+// biases and x 16-byte aligned; mma: the tensor-core kernel may be tried.
+qgemv_gemv_plan route_plain(int bits, int M, long long N, int K, int sms, bool al16, bool mma) {
+  qgemv_gemv_plan r{};
+  r.path = QGEMV_PATH_GENERIC;
+  r.passes = 1;
+  r.cluster = 1;
+  if (M == 1) {
+    const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms);
+    if (p.ok && al16) {
+      r.path = QGEMV_PATH_STREAM;
+      r.stages = p.ns;
+      r.smem_bytes = p.smem_bytes;
+    }
+    return r;
+  }
+  // Small batch on the tensor cores (M >= 3, and M = 2 on short ops): one
+  // pass holding all M rows when their activations fit in shared memory,
+  // else passes of at most 4 rows (a pass of 1 or 2 rows takes the
+  // CUDA-core kernels).
+  int mp = 0, smem = 0, ns = 0, cl = 1, kc = 0;
+  if (al16 && mma && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl, &kc)) {
+    r.path = QGEMV_PATH_MMA;
+  } else if (al16 && mma && M > 4 &&
+             qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns, &cl, &kc)) {
+    r.path = QGEMV_PATH_MMA_PASSES;
+    r.passes = (M + 3) / 4;
+  }
+  if (r.path != QGEMV_PATH_GENERIC) {
+    r.m_pad = mp;
+    r.cluster = cl;
+    r.chunk_k = kc;
+    r.stages = ns;
+    r.smem_bytes = smem;
+    return r;
+  }
+  // CUDA-core small-batch kernel, then the generic kernel.
+  const StreamPlan p = qgemv::make_batch_plan(bits, K, N, M, sms);
+  const StreamPlan p4 = qgemv::make_batch_plan(bits, K, N, 4, sms);
+  if (al16 && p.ok) {
+    r.path = QGEMV_PATH_BATCH;
+    r.stages = p.ns;
+    r.smem_bytes = p.smem_bytes;
+  } else if (al16 && p4.ok) {
+    r.path = QGEMV_PATH_BATCH_PASSES;
+    r.passes = (M + 3) / 4;
+    r.stages = p4.ns;
+    r.smem_bytes = p4.smem_bytes;
+  }
+  return r;
+}
+
 int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const uint16_t* biases,
                const uint16_t* x, uint16_t* y, int M, int N, int K, const uint16_t* residual,
                void* stream) {
@@ -105,65 +158,58 @@ int plain_impl(int bits, const uint32_t* codes, const uint16_t* scales, const ui
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool al16 = aligned(codes, 16) && aligned(scales, 16) && aligned(biases, 16) &&
                     aligned(x, 16);
-  if (M == 1) {
-    const StreamPlan p = qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms);
-    if (p.ok && al16) return finish(qgemv::stream_plain(bits, p, a, st, dev));
-    return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
-  }
-  // Small batch on the tensor cores (M >= 3, and M = 2 on short ops): one
-  // pass holding all M rows when their activations fit in shared memory,
-  // else passes of at most 4 rows (a pass of 1 or 2 rows takes the
-  // CUDA-core kernels).
-  // (cudaErrorNotSupported: the device cannot host the plan's clusters, say
-  // under a restricted SM partition; nothing was launched, so the CUDA-core
-  // kernels below take the call.)
-  int mp = 0, smem = 0, ns = 0, cl = 1;
-  bool mma_ok = al16;
-  if (mma_ok && qgemv::batch_mma_plan(bits, K, N, M, sms, &mp, &smem, &ns, &cl)) {
+  qgemv_gemv_plan r = route_plain(bits, M, N, K, sms, al16, true);
+  if (r.path == QGEMV_PATH_MMA) {
     const cudaError_t e = qgemv::stream_batch_mma(bits, a, sms, st, dev);
+    // cudaErrorNotSupported: the device cannot host the plan's clusters (a
+    // restricted SM partition, say); nothing was launched, so the CUDA-core
+    // kernels take the call.
     if (e != cudaErrorNotSupported) return finish(e);
     cudaGetLastError();
-    mma_ok = false;
+    r = route_plain(bits, M, N, K, sms, al16, false);
   }
-  if (mma_ok && M > 4 && qgemv::batch_mma_plan(bits, K, N, 4, sms, &mp, &smem, &ns, &cl)) {
-    for (int m0 = 0; m0 < M; m0 += 4) {
-      StreamArgs ap = a;
-      ap.M = M - m0 < 4 ? M - m0 : 4;
-      ap.x = a.x + static_cast<size_t>(m0) * K;
-      ap.y = a.y + static_cast<size_t>(m0) * N;
-      if (a.residual) ap.residual = a.residual + static_cast<size_t>(m0) * N;
-      cudaError_t e;
-      if (ap.M >= 3) {
-        e = qgemv::stream_batch_mma(bits, ap, sms, st, dev);
-      } else if (ap.M == 2) {
-        const StreamPlan pm = qgemv::make_batch_plan(bits, K, N, 2, sms);
-        e = pm.ok ? qgemv::stream_batch(bits, pm, ap, st, dev)
-                  : qgemv::generic_launch(qgemv::kPlain, bits, ap, st);
-      } else {
-        e = launch_single_row(bits, ap, sms, st, dev);
+  auto pass = [&](int m0) {
+    StreamArgs ap = a;
+    ap.M = M - m0 < 4 ? M - m0 : 4;
+    ap.x = a.x + static_cast<size_t>(m0) * K;
+    ap.y = a.y + static_cast<size_t>(m0) * N;
+    if (a.residual) ap.residual = a.residual + static_cast<size_t>(m0) * N;
+    return ap;
+  };
+  switch (r.path) {
+    case QGEMV_PATH_STREAM:
+      return finish(qgemv::stream_plain(
+          bits, qgemv::make_stream_plan(qgemv::kPlain, bits, K, N, 1, sms), a, st, dev));
+    case QGEMV_PATH_MMA_PASSES:
+      for (int m0 = 0; m0 < M; m0 += 4) {
+        const StreamArgs ap = pass(m0);
+        cudaError_t e;
+        if (ap.M >= 3) {
+          e = qgemv::stream_batch_mma(bits, ap, sms, st, dev);
+        } else if (ap.M == 2) {
+          const StreamPlan pm = qgemv::make_batch_plan(bits, K, N, 2, sms);
+          e = pm.ok ? qgemv::stream_batch(bits, pm, ap, st, dev)
+                    : qgemv::generic_launch(qgemv::kPlain, bits, ap, st);
+        } else {
+          e = launch_single_row(bits, ap, sms, st, dev);
+        }
+        if (e != cudaSuccess) return finish(e);
       }
-      if (e != cudaSuccess) return finish(e);
-    }
-    return QGEMV_OK;
+      return QGEMV_OK;
+    case QGEMV_PATH_BATCH:
+      return finish(
+          qgemv::stream_batch(bits, qgemv::make_batch_plan(bits, K, N, M, sms), a, st, dev));
+    case QGEMV_PATH_BATCH_PASSES:
+      for (int m0 = 0; m0 < M; m0 += 4) {
+        const StreamArgs ap = pass(m0);
+        const StreamPlan pp = qgemv::make_batch_plan(bits, K, N, ap.M < 2 ? 2 : ap.M, sms);
+        const cudaError_t e = qgemv::stream_batch(bits, pp, ap, st, dev);
+        if (e != cudaSuccess) return finish(e);
+      }
+      return QGEMV_OK;
+    default:
+      return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
   }
-  // CUDA-core small-batch kernel, then the generic kernel.
-  const StreamPlan p = qgemv::make_batch_plan(bits, K, N, M, sms);
-  if (al16 && p.ok) return finish(qgemv::stream_batch(bits, p, a, st, dev));
-  const StreamPlan p4 = qgemv::make_batch_plan(bits, K, N, 4, sms);
-  if (al16 && p4.ok) {
-    for (int m0 = 0; m0 < M; m0 += 4) {
-      StreamArgs ap = a;
-      ap.M = M - m0 < 4 ? M - m0 : 4;
-      const StreamPlan pp = qgemv::make_batch_plan(bits, K, N, ap.M < 2 ? 2 : ap.M, sms);
-      ap.x = a.x + static_cast<size_t>(m0) * K;
-      ap.y = a.y + static_cast<size_t>(m0) * N;
-      if (a.residual) ap.residual = a.residual + static_cast<size_t>(m0) * N;
-      const cudaError_t e = qgemv::stream_batch(bits, pp, ap, st, dev);
-      if (e != cudaSuccess) return finish(e);
-    }
-    return QGEMV_OK;
-  }
-  return finish(qgemv::generic_launch(qgemv::kPlain, bits, a, st));
 }
 
 }  // namespace
@@ -508,6 +554,15 @@ int qgemv_lm_head_sample(const uint32_t* codes, const uint16_t* scales, const ui
   return finish(qgemv::sample_topk_launch(reinterpret_cast<const __half*>(logits), N, top_k,
                                           temperature, u, token, topk_idx, topk_prob,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+int qgemv_plan_gemv(int bits, int M, int N, int K, int sms, int aligned16, qgemv_gemv_plan* out) {
+  if (!out) return QGEMV_ENULL;
+  if ((bits != 2 && bits != 4 && bits != 8) || M < 1 || M > QGEMV_MAX_M || N < 1 ||
+      !valid_k(K) || sms < 1)
+    return QGEMV_EINVAL;
+  *out = route_plain(bits, M, N, K, sms, aligned16 != 0, true);
+  return QGEMV_OK;
 }
 
 int qgemv_lut4(const uint32_t* codes, const uint16_t* lut, int n_luts, int rows_per_lut,

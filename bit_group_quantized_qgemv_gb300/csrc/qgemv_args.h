@@ -231,13 +231,15 @@ cudaError_t stream_moe_down(const StreamPlan& p, const StreamArgs& a, cudaStream
                             int device);
 cudaError_t stream_batch(int bits, const StreamPlan& p, const StreamArgs& a, cudaStream_t st,
                          int device);
-// Tensor-core small-batch kernel (M = 3..8 in one pass, K split across a
-// cluster of up to 4 CTAs when the activations are large).  batch_mma_plan:
-// whether a pass of M rows fits (K a multiple of 512, the staged activations
-// within their shared-memory budget); stream_batch_mma returns
-// cudaErrorNotSupported when it does not.
+// Tensor-core small-batch kernel (M = 3..8, and M = 2 on short ops, in one
+// pass; K split across a cluster of up to 4 CTAs when the activations are
+// large).  batch_mma_plan: whether it takes a pass of M rows (K a multiple
+// of 512, the staged activations within their shared-memory budget), with
+// its B columns, dynamic shared memory, ring depth, cluster size and chunk
+// length (kc nullable); stream_batch_mma returns cudaErrorNotSupported when
+// it does not.
 bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp, int* smem, int* ns,
-                    int* cl);
+                    int* cl, int* kc = nullptr);
 cudaError_t stream_batch_mma(int bits, const StreamArgs& a, int sms, cudaStream_t st, int device);
 cudaError_t stream_argmax(const StreamPlan& p, const StreamArgs& a, cudaStream_t st, int device);
 // Single-CTA argmax of an fp16 vector (the fallback when the streaming kernel

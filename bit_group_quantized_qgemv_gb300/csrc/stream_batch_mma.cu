@@ -794,7 +794,7 @@ cudaError_t launch_mma_t(const StreamArgs& a, MmaGeom gm, const CUtensorMap* map
 // the shape does not fit (K not a multiple of 512, or the staged
 // activations above their budget).
 bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, int* smem_out,
-                    int* ns_out, int* cl_out) {
+                    int* ns_out, int* cl_out, int* kc_out) {
   if ((bits != 4 && bits != 2) || M < kMmaMinM || M > kMaxM || N < 1 || sms < 1) return false;
   if (M == 2 && (K > 4096 || N * (static_cast<long long>(K) * bits / 8 + K / 32) > kMma2Bytes * sms))
     return false;
@@ -816,6 +816,7 @@ bool batch_mma_plan(int bits, int K, long long N, int M, int sms, int* mp_out, i
   *smem_out = kAlignSlack + ns * stage + xs_bytes + kRedBytes;
   *ns_out = ns;
   *cl_out = cl;
+  if (kc_out != nullptr) *kc_out = kc;
   return true;
 }
 

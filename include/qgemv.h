@@ -108,6 +108,36 @@ int qgemv_w8g64(const uint32_t *codes, const uint16_t *scales, const uint16_t *b
                 const uint16_t *residual, void *stream);
 
 /*
+ * qgemv_plan_gemv -- which kernels qgemv_w4g64 / qgemv_w2g64 / qgemv_w8g64
+ * launch for a shape, without touching the device (host-only; for callers
+ * that size work or check a deployment, and for the host tests).  bits 2,
+ * 4 or 8; M, N, K as those calls check them; sms: the device's
+ * multiprocessor count; aligned16: 1 when codes, scales, biases and x are
+ * 16-byte aligned (the fast kernels need it), else 0.  Fills *out:
+ *   path        QGEMV_PATH_* below
+ *   passes      launches of that kernel (passes of at most 4 batch rows)
+ *   m_pad       tensor-core paths: B columns the batch is padded to (4, 8)
+ *   cluster     tensor-core paths: CTAs that split K between them (1, 2, 4)
+ *   chunk_k     tensor-core paths: k per ring stage
+ *   stages      ring depth of the kernel (0 for the generic kernel)
+ *   smem_bytes  its dynamic shared memory per CTA (0 for the generic kernel)
+ * The tensor-core path can still fall back to the CUDA-core kernels at
+ * launch when the device cannot host the plan's clusters.  Returns
+ * QGEMV_ENULL (out NULL) or QGEMV_EINVAL (bits, M, N, K or sms out of
+ * range), else QGEMV_OK.
+ */
+#define QGEMV_PATH_GENERIC 0      /* one thread block per 8 rows, any alignment */
+#define QGEMV_PATH_STREAM 1       /* M = 1 streaming kernel */
+#define QGEMV_PATH_MMA 2          /* tensor-core small batch, one pass */
+#define QGEMV_PATH_MMA_PASSES 3   /* tensor-core small batch, passes of <= 4 rows */
+#define QGEMV_PATH_BATCH 4        /* CUDA-core small batch, one pass */
+#define QGEMV_PATH_BATCH_PASSES 5 /* CUDA-core small batch, passes of <= 4 rows */
+typedef struct {
+  int path, passes, m_pad, cluster, chunk_k, stages, smem_bytes;
+} qgemv_gemv_plan;
+int qgemv_plan_gemv(int bits, int M, int N, int K, int sms, int aligned16, qgemv_gemv_plan *out);
+
+/*
  * rmsnorm_qgemv -- y = W . (x * gamma / sqrt(mean(x^2) + eps)), M = 1,
  * 4-bit g64.  The RMSNorm + QKV matvec fusion of INFERENCE_RESEARCH.md
  * section 1 (and the RMS normalisation shader on the hada.io page).

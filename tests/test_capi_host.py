@@ -219,3 +219,67 @@ def test_expert_byte_accounting_pins_group64_fp16():
     # 8B layer total from the matvec shapes
     assert sum(acc.weight_bytes(n, k, 4) for n, k in
                [(6144, 4096), (4096, 4096), (2 * 14336, 4096), (4096, 14336)]) == 122683392
+
+
+def _plan(q, bits, M, N, K, sms=152, aligned16=True):
+    return q.plan_gemv(bits, M, N, K, sms, aligned16)
+
+
+def test_gemv_routing_by_batch_and_shape(q):
+    """qgemv_plan_gemv (host-only) pins the routing of qgemv_w4g64 / w2g64 /
+    w8g64: M = 1 streams; M >= 3 and short M = 2 ops take the tensor cores;
+    long M = 2 ops the CUDA-core small-batch kernel; 8-bit batches and
+    misaligned operands the generic kernel."""
+    assert _plan(q, 4, 1, 4096, 4096)["path"] == "stream"
+    assert _plan(q, 4, 1, 4096, 4096, aligned16=False)["path"] == "generic"
+    assert _plan(q, 4, 4, 4096, 4096, aligned16=False)["path"] == "generic"
+    # M = 2: tensor cores only for K <= 4096 and at most 128 KB of weights per SM
+    assert _plan(q, 4, 2, 4096, 4096)["path"] == "mma"
+    assert _plan(q, 4, 2, 1024, 1024)["path"] == "mma"
+    assert _plan(q, 4, 2, 14336, 4096)["path"] == "batch"   # 217 KB per SM
+    assert _plan(q, 4, 2, 4096, 14336)["path"] == "batch"
+    assert _plan(q, 2, 2, 4096, 4096)["path"] == "mma"
+    for M in (3, 4, 5, 8):
+        for K in (4096, 14336):
+            p = _plan(q, 4, M, 4096, K)
+            assert p["path"] == "mma" and p["passes"] == 1, (M, K, p)
+            assert p["m_pad"] == (4 if M <= 4 else 8)
+    assert _plan(q, 8, 4, 4096, 4096)["path"] == "generic"
+    # K not a multiple of 512 (tensor cores) nor of 1024 (CUDA-core small batch)
+    assert _plan(q, 4, 3, 300, 1088)["path"] == "generic"
+
+
+def test_gemv_tensor_core_cluster_and_stage_plan(q):
+    """The tensor-core plan: K split four ways when a whole row's staged
+    activations exceed 96 KB, chunks of at most 4096 k (the longest that
+    divides the CTA's k range), a ring of at least two stages, all within the
+    227 KB of shared memory a block may take."""
+    cases = {  # (bits, M, K): (cluster, chunk_k)
+        (4, 4, 4096): (1, 4096), (4, 8, 4096): (1, 4096), (4, 4, 8192): (1, 4096),
+        (4, 8, 8192): (4, 2048), (4, 3, 14336): (4, 3584), (4, 8, 14336): (4, 3584),
+        (4, 4, 16384): (4, 4096), (4, 8, 32768): (4, 4096), (2, 8, 14336): (4, 3584),
+        (4, 4, 1024): (1, 1024),
+    }
+    for (bits, M, K), (cl, kc) in cases.items():
+        p = _plan(q, bits, M, 4096, K)
+        assert p["path"] == "mma", (bits, M, K, p)
+        assert (p["cluster"], p["chunk_k"]) == (cl, kc), (bits, M, K, p)
+        assert (K // cl) % kc == 0 and kc % 512 == 0
+        assert 2 <= p["stages"] <= 16
+        assert p["smem_bytes"] <= 227 * 1024
+        # staged activations per CTA (fragments + group sums) stay within 132 KB
+        mp = p["m_pad"]
+        assert 2 * mp * (K // cl) + (K // cl) // 2 <= 132 * 1024
+    # too long to hold even split four ways, and past the CUDA-core small
+    # batch's K <= 16384: the generic kernel
+    assert _plan(q, 4, 8, 4096, 65536)["path"] == "generic"
+
+
+def test_gemv_plan_arguments(q):
+    out = q._binding.GemvPlan()
+    L = q.lib
+    assert L.qgemv_plan_gemv(4, 4, 4096, 4096, 152, 1, None) == -2
+    for args in [(3, 4, 4096, 4096, 152), (4, 0, 4096, 4096, 152), (4, 9, 4096, 4096, 152),
+                 (4, 4, 0, 4096, 152), (4, 4, 4096, 100, 152), (4, 4, 4096, 4096, 0)]:
+        assert L.qgemv_plan_gemv(*args, 1, ctypes.byref(out)) == -1, args
+    assert L.qgemv_plan_gemv(4, 4, 4096, 4096, 152, 1, ctypes.byref(out)) == 0
