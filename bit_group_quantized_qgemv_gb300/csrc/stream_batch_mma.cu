@@ -1,7 +1,7 @@
 // stream_batch_mma.cu -- small-batch GEMV on the tensor cores,
-// Y[m] = W . X[m] (+ R[m]) for M = 2..8 activation rows (INFERENCE_RESEARCH.md
-// section 1: routing by M; the weights are loaded once and applied to every
-// row of the batch).
+// Y[m] = W . X[m] (+ R[m]) for M = 3..8 activation rows, and M = 2 on short
+// ops (INFERENCE_RESEARCH.md section 1: routing by M; the weights are loaded
+// once and applied to every row of the batch).
 //
 // At M > 1 the product is a real (if thin) dense contraction: every decoded
 // weight meets M activations, and on CUDA cores the M fp32 FMAs per weight
@@ -122,9 +122,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 2-D TMA copy of one box (x: byte column, y: row) into this CTA's shared
-// memory, completion counted on `bar`.
-// A 3-D box {x, y, z} of a tensor map into shared memory.
+// A 3-D box {x, y, z} of a tensor map into this CTA's shared memory,
+// completion counted on `bar`.
 __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                          uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -134,6 +133,7 @@ __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// A 2-D box (x: byte column, y: row), likewise.
 __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y,
                                         uint32_t bar, uint64_t policy) {
   asm volatile(
